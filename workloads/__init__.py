@@ -14,6 +14,7 @@ from .gen import (  # noqa: F401
     make_append_batch,
     referenced_tokens,
     all_tokens,
+    redraw_indices,
     bf16_from_f32,
     f32_from_bf16,
 )

@@ -251,3 +251,14 @@ def make_append_batch(wl: Workload, stream: int = 0):
         seq, pos = wl.q_seq.copy(), wl.q_pos.copy()
     lat, rope = make_rows(wl, int(seq.shape[0]), stream=1000 + stream)
     return seq, pos, lat, rope
+
+
+def redraw_indices(wl: Workload, stream: int) -> np.ndarray:
+    """A fresh top-k set per query token for the same sequences (another model layer).
+
+    Same selection rule as the workload's own, drawn from an independent stream.
+    """
+    mode = {"tiny": "uniform", "decode_batch": "sorted", "agent": "recent_mix",
+            "multi_token": "sorted", "append_dense": "all"}[wl.name]
+    rng = _rng(wl.seed, 4, stream)
+    return np.stack([_draw(rng, int(p) + 1, wl.topk, mode) for p in wl.q_pos]).astype(np.int32)
