@@ -177,6 +177,44 @@ int32_t sparse_mla_decode(const void* q_latent, const void* q_rope, const int32_
                           void* workspace, size_t workspace_bytes, int32_t num_splits,
                           int32_t* invalid_count, void* stream);
 
+/*
+ * sparse_mla_decode without a caller-provided workspace. The paper has no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory themselves -- for example a plugin whose host
+ * application owns the device heap through its own allocator and does not
+ * let plugins call cudaMalloc, or a service that fixes its device-memory
+ * budget at start-up.
+ *
+ * Arguments, results and errors are those of sparse_mla_decode, minus
+ * `workspace` / `workspace_bytes`. When the split-K combine needs scratch
+ * (sparse_mla_decode_workspace_size(num_q, num_heads, topk, num_splits) > 0)
+ * it uses a static device buffer of NVFP4_MLA_NOALLOC_SCRATCH_BYTES that
+ * this library defines; shapes needing more return NVFP4_MLA_ERR_WORKSPACE
+ * before anything is enqueued. The entry point allocates nothing and calls
+ * no allocating routine.
+ *   - The buffer lives in every device that loads the library, until the
+ *     process exits (16 MiB each).
+ *   - The first call on a device that needs scratch looks up the buffer's
+ *     device address (cudaGetSymbolAddress, with that device current) and
+ *     caches it; make that first call before any stream capture.
+ *   - Every call shares the one buffer: calls whose work can overlap on the
+ *     GPU (different streams, or different host threads, without ordering
+ *     between them) race on it and corrupt each other's results. Order them
+ *     on one stream. Each call fully writes the scratch it reads, so no
+ *     clearing is needed between calls.
+ */
+#define NVFP4_MLA_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int32_t sparse_mla_decode_noalloc(const void* q_latent, const void* q_rope, const int32_t* q_seq,
+                                  const int32_t* topk_idx, int32_t num_q, int32_t num_heads,
+                                  int32_t topk, const int32_t* block_table, int32_t num_seqs,
+                                  int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                                  int32_t page_size, const void* cache, int64_t num_blocks,
+                                  int64_t block_stride_bytes, int32_t row_format, float sm_scale,
+                                  float latent_scale, float rope_scale, void* out,
+                                  int32_t out_fp32, float* lse, int32_t num_splits,
+                                  int32_t* invalid_count, void* stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

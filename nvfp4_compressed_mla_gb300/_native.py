@@ -25,6 +25,8 @@ SIGNATURES = {
     "sparse_mla_decode_workspace_size": (SZ, [I32, I32, I32, I32]),
     "sparse_mla_decode": (I32, [P, P, P, P, I32, I32, I32, P, I32, I32, P, I32, P, I64, I64, I32,
                                 F32, F32, F32, P, I32, P, P, SZ, I32, P, P]),
+    "sparse_mla_decode_noalloc": (I32, [P, P, P, P, I32, I32, I32, P, I32, I32, P, I32, P, I64,
+                                        I64, I32, F32, F32, F32, P, I32, P, I32, P, P]),
 }
 
 

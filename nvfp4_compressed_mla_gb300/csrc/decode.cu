@@ -22,6 +22,8 @@
 //   6. O += P V over the 512 latent dims (each warp owns 64 of them).
 #include <math.h>
 
+#include <atomic>
+
 #include "common.cuh"
 
 namespace nvfp4_mla {
@@ -583,4 +585,63 @@ extern "C" int32_t sparse_mla_decode(
     return launch_status();
   }
   return NVFP4_MLA_OK;
+}
+
+// ------------------------------------------------------------------------
+// Decode for callers that cannot allocate device memory: the split-K
+// scratch is a static device array of this translation unit instead of a
+// caller workspace. Its device address is looked up once per device (with
+// that device current) and cached; the first call on a device therefore
+// belongs before any stream capture. Concurrent calls share the array and
+// race; each call writes every scratch element it later reads.
+namespace nvfp4_mla {
+namespace {
+constexpr size_t kNoAllocScratch = NVFP4_MLA_NOALLOC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch];
+constexpr int kScratchDevices = 64;
+std::atomic<uintptr_t> g_noalloc_ptr[kScratchDevices];
+
+int32_t noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchDevices) {
+    cudaGetLastError();
+    return NVFP4_MLA_ERR_DEVICE;
+  }
+  uintptr_t p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p == 0) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+      cudaGetLastError();
+      return NVFP4_MLA_ERR_LAUNCH;
+    }
+    p = reinterpret_cast<uintptr_t>(addr);
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = reinterpret_cast<void*>(p);
+  return NVFP4_MLA_OK;
+}
+}  // namespace
+}  // namespace nvfp4_mla
+
+extern "C" int32_t sparse_mla_decode_noalloc(
+    const void* q_latent, const void* q_rope, const int32_t* q_seq, const int32_t* topk_idx,
+    int32_t num_q, int32_t num_heads, int32_t topk, const int32_t* block_table, int32_t num_seqs,
+    int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t page_size, const void* cache,
+    int64_t num_blocks, int64_t block_stride_bytes, int32_t row_format, float sm_scale,
+    float latent_scale, float rope_scale, void* out, int32_t out_fp32, float* lse,
+    int32_t num_splits, int32_t* invalid_count, void* stream) {
+  void* scratch = nullptr;
+  if (num_q > 0 && shape_ok(num_q, num_heads, topk) && num_splits >= 0 && num_splits <= 64) {
+    const size_t need = sparse_mla_decode_workspace_size(num_q, num_heads, topk, num_splits);
+    if (need == SIZE_MAX) return NVFP4_MLA_ERR_DEVICE;
+    if (need > kNoAllocScratch) return NVFP4_MLA_ERR_WORKSPACE;
+    if (need > 0) {
+      if (int32_t st = noalloc_scratch(&scratch)) return st;
+    }
+  }
+  return sparse_mla_decode(q_latent, q_rope, q_seq, topk_idx, num_q, num_heads, topk, block_table,
+                           num_seqs, max_blocks_per_seq, seq_lens, page_size, cache, num_blocks,
+                           block_stride_bytes, row_format, sm_scale, latent_scale, rope_scale, out,
+                           out_fp32, lse, scratch, scratch ? kNoAllocScratch : 0, num_splits,
+                           invalid_count, stream);
 }
