@@ -162,7 +162,7 @@ size_t sparse_mla_decode_workspace_size(int32_t num_q, int32_t num_heads, int32_
  *                bytes for the same shape and num_splits (may be NULL when
  *                that size is 0); scratch, contents need not be initialised
  *   num_splits   0 = automatic; otherwise 1..64, clamped to the number of
- *                64-slot tiles in topk
+ *                128-slot tiles in topk
  *   invalid_count nullable device int32 (accumulated with atomicAdd)
  * Duplicate entries count once each. The result does not depend on the
  * order of entries within a row of topk_idx beyond fp32 rounding.

@@ -5,7 +5,7 @@
 
 namespace nvfp4_mla {
 
-constexpr int kTile = 64;            // top-k slots per pipeline tile
+constexpr int kTile = 128;           // top-k slots per pipeline tile (two 64-slot sub-tiles)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 

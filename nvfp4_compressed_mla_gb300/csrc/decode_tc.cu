@@ -4,40 +4,44 @@
 // describes a kernel that gathers the compressed rows at the indexer's
 // positions, dequantises them on chip, runs FP16 MMAs with FP32
 // accumulation, lets separate warp groups dequantise / score / accumulate
-// through a three-slot buffer, and merges a query token's partial results
+// through a multi-slot buffer, and merges a query token's partial results
 // across a cluster of SMs. This kernel keeps those ideas and reshapes them
-// for tcgen05 and its 256 KB of tensor memory per SM.
+// for tcgen05 and its 512 columns of tensor memory per SM.
 //
 // With 128 heads, one query token's resident state does not fit one SM:
 // Q (128 x 576 FP16) and O (128 x 512 FP32, all 512 TMEM columns) together
-// exceed both TMEM and shared memory. So each (token, split) unit is a
-// 2-CTA cluster that splits the two contractions between two SMs:
+// exceed both TMEM and shared memory. Each (token, split) unit is a 2-CTA
+// cluster that splits the two contractions between two SMs:
 //
-//   rank 0, "score" CTA: Q lives in TMEM (288 columns, the A operand).
-//     Per 64-row tile: S = Q K^T (M=128 heads, N=64 tokens, K=576) into one of
-//     two 64-column TMEM score buffers; four softmax warps (one thread per
-//     head) read S, keep the running max / sum, and write P (FP16, 128 x 64)
-//     straight into the peer's shared memory.
-//   rank 1, "output" CTA: O lives in TMEM (512 columns).
-//     Per tile: O += P V (M=128, N=2 x 256 latent dims, K=64 tokens), with P
-//     and V^T from shared memory. Four correction warps rescale O when the
-//     score CTA raises its reference max, forward "P buffer free" back, and
-//     write the normalised output at the end.
+//   rank 0, "score" CTA: Q_latent lives in TMEM (256 columns, the MMA's A
+//     operand) and Q_rope in shared memory. Per 128-row tile, S = Q K^T
+//     (M=128 heads, N=128 rows) accumulates into one of two 128-column TMEM
+//     buffers, fed by 64-dim chunks of K (128 rows x 64 dims FP16) that the
+//     dequant warps write into a 4-slot ring: 8 latent chunks with A from
+//     TMEM, then the rope chunk with A from shared memory. N=128 keeps each
+//     MMA well above the tensor core's per-instruction floor, and the chunk
+//     ring bounds shared memory independently of the tile width.
+//     Four softmax warps (one thread per head) read S in two 64-row halves,
+//     keep a lazy reference max and the running sum, stage P (FP16) with the
+//     rescale factors locally and bulk-copy them into the peer's memory.
+//   rank 1, "output" CTA: O lives in TMEM (512 columns). Per 64-row
+//     sub-tile: O += P V (M=128, N=2 x 256 latent dims, K=64 rows), P and V^T
+//     from shared memory. Four correction warps rescale O when the score CTA
+//     raised its reference max, hand P buffers back, and write the
+//     normalised output at the end.
 //
-// Both CTAs run the same gather/dequant pipeline on their own copy of the
-// rows: a producer warp resolves the top-k slots through the block table
-// (-1 and unresolvable slots are skipped: no load is issued) and issues one
-// bulk copy (cp.async.bulk) per row into a 3-stage raw ring; eight dequant
-// warps expand E2M1 x E4M3 (exact in FP16) into the 128-byte-swizzled
-// K-major layout the MMA reads: the score CTA writes K [token][576], the
-// output CTA writes V^T [512][token]. One thread issues the MMAs; commits
-// signal mbarriers. Softmax uses a lazy reference max: P = 2^(s - m_ref)
-// with m_ref raised only when a score exceeds it by more than 8 (P <= 256
-// in FP16), so O needs rescaling only on those (rare) tiles.
+// Both CTAs gather their own copy of the rows: a producer warp resolves
+// top-k slots through the block table (-1 and unresolvable slots issue no
+// load), keeping the index and block-table loads two sub-tiles ahead, and
+// copies each row in 16-byte cp.async pieces into a ring of 64-row stages. Eight dequant warps expand E2M1 x E4M3 (exact in FP16) into the
+// 128-byte-swizzled K-major layouts the MMAs read. One thread issues the
+// MMAs; commits signal mbarriers. Softmax: P = 2^(s - m_ref) with m_ref
+// raised only when a score exceeds it by more than 8 (so P <= 256 in FP16)
+// and O rescaled only on those (rare) sub-tiles.
 //
 // Every wait is bounded (about a second of clock64 cycles); a wait that
-// runs out sets an abort flag, the CTAs unwind, free TMEM, and the unit's
-// outputs are written as NaN.
+// runs out sets an abort flag, the roles unwind together, tensor memory is
+// freed, and the unit's outputs are written as NaN.
 #include <math.h>
 
 #include "decode_common.cuh"
@@ -45,54 +49,66 @@
 namespace nvfp4_mla {
 namespace {
 
+constexpr int kSub = 64;             // rows per gather stage / P sub-tile
 constexpr int kWarps = 14;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDequantWarp0 = 6;
-constexpr int kDequantThreads = 256;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kQCol = 0;      // score CTA: Q, 288 columns
-constexpr uint32_t kSCol = 384;    // score CTA: score buffers at 384 and 448
-constexpr float kTau = 8.0f;       // lazy rescale threshold (log2 units)
+constexpr uint32_t kSCol = 256;      // score CTA: S buffers at columns 256 and 384
+constexpr int kChunkSlots = 4;
+constexpr int kChunksPerTile = 9;    // 8 latent + 1 rope
+constexpr float kTau = 8.0f;         // lazy rescale threshold (log2 units)
 constexpr long long kWaitCycles = 1ll << 31;
-constexpr uint32_t kIdescQK = (1u << 4) | ((64u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kIdescPV = (1u << 4) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kAFBytes = 528;   // per P buffer: 128 fp32 rescale factors + 4 warp flags
 
 template <int kFmt>
 struct TcLayout {
   static constexpr bool kNv = kFmt == NVFP4_MLA_ROW_NVFP4_352;
   static constexpr int kRowBytes = kNv ? kNvfp4Row : kFp8Row;
-  static constexpr int kCopyS = kRowBytes;           // score CTA copies whole rows
-  static constexpr int kCopyO = kNv ? 288 : 512;     // output CTA: latent part only
-  static constexpr int kStages = kNv ? 3 : 2;
-  static constexpr int kPad = 16;                    // per 8-row group, against bank conflicts
-  static constexpr int kStageS = kTile * kCopyS + 8 * kPad;
-  static constexpr int kStageO = kTile * kCopyO + 8 * kPad;
-  static constexpr int kKTile = 9 * 8192;            // 64 tokens x 576 FP16, 9 K-blocks of 64
-  static constexpr int kRawS = 2 * kKTile;
-  static constexpr int kEndS = kRawS + kStages * kStageS;
-  static constexpr int kVTile = 64 * 1024;           // 512 dims x 64 tokens FP16
-  static constexpr int kPTile = 16 * 1024;           // 128 heads x 64 tokens FP16
+  static constexpr int kCopyS = kRowBytes;        // score CTA copies whole rows
+  static constexpr int kCopyO = kNv ? 288 : 512;  // output CTA: latent part (+ scales)
+  static constexpr int kPad = 16;                 // per 8-row group, against bank conflicts
+  static constexpr int kStageS = kSub * kCopyS + 8 * kPad;
+  static constexpr int kStageO = kSub * kCopyO + 8 * kPad;
+  static constexpr int kStagesS = kNv ? 4 : 3;
+  static constexpr int kStagesO = kNv ? 3 : 2;
+  // score CTA
+  static constexpr int kChunk = 16384;            // 128 rows x 64 dims FP16
+  static constexpr int kQRope = kChunkSlots * kChunk;
+  static constexpr int kPStage = kQRope + 16384;  // 2 x [P 16 KB][rescale + flags]
+  static constexpr int kPStageStride = 17408;
+  static constexpr int kRawS = kPStage + 2 * kPStageStride;
+  static constexpr int kEndS = kRawS + kStagesS * kStageS;
+  static constexpr int kQStage = 0;               // start-up: Q (bf16) staged over the above
+  static constexpr int kQStageBytes = 128 * (kLatent + kRope) * 2;
+  // output CTA
+  static constexpr int kVTile = 64 * 1024;        // 512 dims x 64 rows FP16
+  static constexpr int kPTile = 16 * 1024;        // 128 heads x 64 rows FP16
   static constexpr int kP = 2 * kVTile;
   static constexpr int kRawO = kP + 2 * kPTile;
-  static constexpr int kEndO = kRawO + kStages * kStageO;
+  static constexpr int kEndO = kRawO + kStagesO * kStageO;
   static constexpr int kCtl = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
   static constexpr int kCtlBytes = 2560;
   static constexpr int kBytes = kCtl + kCtlBytes;
   static_assert(kBytes <= 232448, "shared memory budget");
-  static_assert(kStageS % 16 == 0 && kStageO % 16 == 0 && kCopyO % 16 == 0, "bulk copy alignment");
+  static_assert(kQStageBytes <= kEndS, "Q staging fits the score CTA's buffers");
+  static_assert(kStageS % 16 == 0 && kStageO % 16 == 0, "bulk copy alignment");
 };
 
-// control block (same offset in both CTAs of the cluster)
+// control block: same offset in both CTAs of the cluster
 struct Ctl {
-  static constexpr int kRawFull = 0, kRawEmpty = 24, kTileFull = 48, kTileEmpty = 64,
-                       kSFull = 80, kSEmpty = 96, kPFull = 112, kPEmpty = 128, kPvDone = 144,
-                       kOCorr = 160, kStats = 168, kQReady = 176, kTmem = 192, kAbort = 196,
-                       kStageMask = 200, kMaskRing = 224, kFlags = 288, kAlpha = 320,
-                       kFinalM = 1344, kFinalL = 1856, kEnd = 2368;
+  static constexpr int kRawFull = 0, kRawEmpty = 32, kChunkFull = 64, kChunkEmpty = 96,
+                       kVtFull = 128, kVtEmpty = 144, kSFull = 160, kSEmpty = 176, kPFull = 192,
+                       kPEmpty = 208, kPvDone = 224, kOCorr = 240, kStats = 248, kQReady = 256,
+                       kQFull = 264, kTmem = 272, kAbort = 276, kStageMask = 280,
+                       kMaskRing = 312, kAF = 448, kFinalM = 1504, kFinalL = 2016, kEnd = 2528;
 };
 static_assert(Ctl::kEnd <= TcLayout<NVFP4_MLA_ROW_NVFP4_352>::kCtlBytes, "control block");
+static_assert(Ctl::kAF + 2 * kAFBytes <= Ctl::kFinalM, "rescale/flag slots");
 
 // ------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -143,20 +159,11 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                              uint32_t d) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
-               "r"(c), "r"(d)
-               : "memory");
-}
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_cta() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -277,6 +284,51 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::
+                   "r"(cluster_bar),
+               "r"(bytes)
+               : "memory");
+}
+// shared (this CTA) -> shared (cluster peer), completion counted on the peer's mbarrier
+__device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                         uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
+}
+// The barrier's arrival by this thread fires once all of its earlier cp.async
+// copies have completed (the arrival is one of the barrier's expected count).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Barrier 1 over the 128 threads of warps 0-3, returning the AND of `v` over them.
+__device__ __forceinline__ bool group_and(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\n"
+      "bar.red.and.pred q, 1, 128, p;\nselp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
@@ -285,13 +337,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
-// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte
-// swizzled K-major tile whose rows are 128 bytes (8-row groups of 1024 B).
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `row` in a 128-byte
+// swizzled K-major tile with 128-byte rows (8-row groups of 1024 bytes).
 __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
   return (row >> 3) * 1024u + (row & 7u) * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
-// Bounded wait; false when it ran out (or another thread aborted already).
+// Bounded wait; false when it ran out (or another thread of the CTA aborted).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t abort_addr) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
@@ -305,22 +357,40 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t
   }
 }
 
-// Warp-uniform bounded wait: every lane waits (and so acquires), and the
+// Warp-uniform bounded wait: every lane waits (and so acquires) and the
 // warp leaves together, so warp-collective operations after it stay converged.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t abort_addr) {
   return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_addr));
 }
 
-// Bounded wait that ignores the abort flag: used to drain issued MMAs
-// before the tensor memory is freed.
+// Bounded wait that ignores the abort flag: drains issued MMAs before the
+// tensor memory is freed.
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   const long long t0 = clock64();
   while (!mbar_test(bar, parity) && clock64() - t0 < kWaitCycles) {
   }
 }
 
-__device__ __forceinline__ uint32_t raw_row_off(int t, int copy) {
-  return static_cast<uint32_t>(t * copy + (t >> 3) * 16);
+__device__ __forceinline__ uint32_t raw_row_off(int r, int copy) {
+  return static_cast<uint32_t>(r * copy + (r >> 3) * 16);
+}
+
+// FP16x2 of two fp32 p values and the conversions of the Q rows.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, float m) {
+  return make_uint4(pack_f16x2(bf16_lo(x.x) * m, bf16_hi(x.x) * m),
+                    pack_f16x2(bf16_lo(x.y) * m, bf16_hi(x.y) * m),
+                    pack_f16x2(bf16_lo(x.z) * m, bf16_hi(x.z) * m),
+                    pack_f16x2(bf16_lo(x.w) * m, bf16_hi(x.w) * m));
+}
+
+// E4M3 bytes (16) -> FP16 (16 values = two 16-byte chunks)
+__device__ __forceinline__ void e4m3x16_to_f16(uint4 v, uint32_t (&h)[8]) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] & 0xFFFFu));
+    h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
+  }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -340,27 +410,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int t = unit / p.num_splits;
   const int tile0 = split * p.tiles_per_split;
   const int n_tiles = min(p.tiles_per_split, p.num_tiles - tile0);
+  const int n_sub = 2 * n_tiles;
 
   auto bar = [&](int off, int i) { return ctl + off + 8u * static_cast<uint32_t>(i); };
   const uint32_t abort_addr = ctl + Ctl::kAbort;
+  const int stages = rank == 0 ? L::kStagesS : L::kStagesO;
 
   if (tid == 0) {
-    for (int s = 0; s < L::kStages; ++s) {
-      mbar_init(bar(Ctl::kRawFull, s), 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(bar(Ctl::kRawFull, s), 32);
       mbar_init(bar(Ctl::kRawEmpty, s), 8);
     }
+    for (int s = 0; s < kChunkSlots; ++s) {
+      mbar_init(bar(Ctl::kChunkFull, s), 8);
+      mbar_init(bar(Ctl::kChunkEmpty, s), 1);
+    }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar(Ctl::kTileFull, s), 8);
-      mbar_init(bar(Ctl::kTileEmpty, s), 1);
+      mbar_init(bar(Ctl::kVtFull, s), 8);
+      mbar_init(bar(Ctl::kVtEmpty, s), 1);
       mbar_init(bar(Ctl::kSFull, s), 1);
       mbar_init(bar(Ctl::kSEmpty, s), 128);
-      mbar_init(bar(Ctl::kPFull, s), 128);
+      mbar_init(bar(Ctl::kPFull, s), 1);
       mbar_init(bar(Ctl::kPEmpty, s), 128);
       mbar_init(bar(Ctl::kPvDone, s), 1);
     }
     mbar_init(bar(Ctl::kOCorr, 0), 128);
     mbar_init(bar(Ctl::kStats, 0), 128);
     mbar_init(bar(Ctl::kQReady, 0), 128);
+    mbar_init(bar(Ctl::kQFull, 0), 1);
     st_shared_u32(abort_addr, (sbase & 1023u) != 0 ? 1u : 0u);
     fence_mbar_init();
   }
@@ -379,228 +456,311 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t stage_bytes = rank == 0 ? L::kStageS : L::kStageO;
 
   if (warp == kProducerWarp) {
-    // ---------------------------------------------- gather: slots -> rows -> ring
-    for (int i = 0; i < n_tiles; ++i) {
-      const int s = i % L::kStages;
-      const uint32_t k = i / L::kStages;
-      if (!warp_wait(bar(Ctl::kRawEmpty, s), (k & 1u) ^ 1u, abort_addr)) break;
-      int64_t off[2];
-      bool val[2];
-      int bad = 0;
+    // ------------------------------------------------ gather: slots -> rows -> stages
+    // Index and block-table loads are dependent global loads. They run two
+    // stages ahead of the copies through a register ring that is indexed by
+    // compile-time slots (the loop is unrolled by the ring length), so no
+    // register hand-off waits on a load still in flight.
+    const bool seq_ok = b >= 0 && b < p.num_seqs;
+    const int32_t* bt_row = p.block_table + static_cast<int64_t>(seq_ok ? b : 0) * p.max_blocks;
+    auto load_pos = [&](int u, int32_t (&pos)[2]) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int slot = (tile0 + i) * kTile + lane + 32 * j;
-        off[j] = -1;
-        if (slot < p.topk) {
-          const int32_t pos = __ldg(idx_row + slot);
-          if (pos != -1) {
-            off[j] = resolve_row(b, pos, len, p.block_table, p.num_seqs, p.max_blocks,
-                                 p.page_size, p.num_blocks, p.block_stride, L::kRowBytes);
-            bad += off[j] < 0;
-          }
-        }
-        val[j] = off[j] >= 0;
+        const int slot = tile0 * kTile + u * kSub + lane + 32 * j;
+        pos[j] = (u < n_sub && slot < p.topk) ? __ldg(idx_row + slot) : -1;
       }
-      const uint32_t b0 = __ballot_sync(0xffffffffu, val[0]);
-      const uint32_t b1 = __ballot_sync(0xffffffffu, val[1]);
-      const uint64_t mask = (static_cast<uint64_t>(b1) << 32) | b0;
-      if (rank == 0) {
-        bad = __reduce_add_sync(0xffffffffu, bad);
-        if (lane == 0 && bad > 0 && p.invalid_count != nullptr) atomicAdd(p.invalid_count, bad);
-      }
-      if (lane == 0) {
-        *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * s) = mask;
-        if (rank == 0)
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (i & 7)) =
-              mask;
-        mbar_arrive_tx(bar(Ctl::kRawFull, s), (__popc(b0) + __popc(b1)) * copy);
-      }
-      __syncwarp();
+    };
+    // page of a position: >= 0, -1 for an empty slot, -2 when it does not resolve
+    auto load_page = [&](const int32_t (&pos)[2], int64_t (&pg)[2]) {
 #pragma unroll
-      for (int j = 0; j < 2; ++j)
-        if (val[j])
-          bulk_g2s(raw_base + s * stage_bytes + raw_row_off(lane + 32 * j, copy),
-                   p.cache + off[j], copy, bar(Ctl::kRawFull, s));
+      for (int j = 0; j < 2; ++j) {
+        const int32_t ps = pos[j];
+        if (ps == -1) {
+          pg[j] = -1;
+        } else if (!seq_ok || ps < 0 || ps >= len || ps / p.page_size >= p.max_blocks) {
+          pg[j] = -2;
+        } else {
+          const int64_t e = __ldg(bt_row + ps / p.page_size);
+          pg[j] = (e < 0 || e >= p.num_blocks) ? -2 : e;
+        }
+      }
+    };
+    const bool go = rank != 0 || warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
+    int32_t posr[6][2];
+    int64_t pgr[3][2];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load_pos(u, posr[u]);
+    load_page(posr[0], pgr[0]);
+    load_page(posr[1], pgr[1]);
+    bool stop = !go;
+    for (int u0 = 0; u0 < n_sub && !stop; u0 += 6) {
+#pragma unroll
+      for (int du = 0; du < 6; ++du) {
+        const int u = u0 + du;
+        if (u >= n_sub) {
+          stop = true;
+          break;
+        }
+        load_pos(u + 4, posr[(du + 4) % 6]);
+        load_page(posr[(du + 2) % 6], pgr[(du + 2) % 3]);
+        const int s = u % stages;
+        const uint32_t k = u / stages;
+        if (!warp_wait(bar(Ctl::kRawEmpty, s), (k & 1u) ^ 1u, abort_addr)) {
+          stop = true;
+          break;
+        }
+        int64_t off[2];
+        bool val[2];
+        int bad = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const int64_t pg = pgr[du % 3][j];
+          off[j] = pg >= 0 ? pg * p.block_stride +
+                                 static_cast<int64_t>(posr[du % 6][j] % p.page_size) * L::kRowBytes
+                           : -1;
+          val[j] = off[j] >= 0;
+          bad += pg == -2;
+        }
+        const uint32_t b0 = __ballot_sync(0xffffffffu, val[0]);
+        const uint32_t b1 = __ballot_sync(0xffffffffu, val[1]);
+        const uint64_t mask = (static_cast<uint64_t>(b1) << 32) | b0;
+        if (rank == 0) {
+          bad = __reduce_add_sync(0xffffffffu, bad);
+          if (lane == 0 && bad > 0 && p.invalid_count != nullptr) atomicAdd(p.invalid_count, bad);
+        }
+        if (lane == 0) {
+          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * s) = mask;
+          if (rank == 0)
+            *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 15)) =
+                mask;
+        }
+        // Each lane copies its own two rows in 16-byte cp.async pieces on the
+        // load/store path (one bulk copy per 352-byte row serialises on the
+        // copy engine); the stage's barrier completes when every lane's copies
+        // have landed.
+        const uint32_t dst0 = raw_base + s * stage_bytes + raw_row_off(lane, copy);
+        const uint32_t dst1 = raw_base + s * stage_bytes + raw_row_off(lane + 32, copy);
+        const uint8_t* src0 = p.cache + (val[0] ? off[0] : 0);
+        const uint8_t* src1 = p.cache + (val[1] ? off[1] : 0);
+        for (int c = 0; c < copy; c += 16) {
+          if (val[0]) cp_async16(dst0 + c, src0 + c);
+          if (val[1]) cp_async16(dst1 + c, src1 + c);
+        }
+        cp_async_arrive_noinc(bar(Ctl::kRawFull, s));
+      }
     }
-  } else if (warp >= kDequantWarp0) {
-    // ---------------------------------------------- dequant: raw -> FP16 swizzled tiles
+  } else if (warp >= kDequantWarp0 && rank == 0) {
+    // ------------------------------------------------ score CTA dequant: K chunks
+    // Chunk kb of tile i: rows 0..127 of the tile x dims [64 kb, 64 kb + 64)
+    // (kb = 8: the 64 rope dims). Thread -> (row, half of the chunk's dims).
     const int dt = tid - kDequantWarp0 * 32;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int s = i % L::kStages;
-      const uint32_t k = i / L::kStages;
-      const int s2 = i & 1;
-      const uint32_t k2 = i >> 1;
-      if (!warp_wait(bar(Ctl::kRawFull, s), k & 1u, abort_addr)) break;
-      if (!warp_wait(bar(Ctl::kTileEmpty, s2), (k2 & 1u) ^ 1u, abort_addr)) break;
+    const int row = dt & 127;
+    const int hf = dt >> 7;
+    bool run = warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
+    for (int i = 0; i < n_tiles && run; ++i) {
+      const int ua = 2 * i, ub = 2 * i + 1;
+      const int sa = ua % L::kStagesS, sb = ub % L::kStagesS;
+      if (!warp_wait(bar(Ctl::kRawFull, sa), (ua / L::kStagesS) & 1u, abort_addr) ||
+          !warp_wait(bar(Ctl::kRawFull, sb), (ub / L::kStagesS) & 1u, abort_addr))
+        break;
+      const int sr = row < kSub ? sa : sb;
       const uint64_t mask =
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * s);
-      const uint32_t raw = raw_base + s * stage_bytes;
-      if (rank == 0) {
-        // K tile [64 tokens][576], 9 K-blocks of 64 dims (8192 B each)
-        const uint32_t ktile = sbase + s2 * L::kKTile;
-        for (int it = dt; it < kTile * 36; it += kDequantThreads) {
-          const int tok = it & 63;
-          const int c16 = it >> 6;  // 16-value group 0..35 (32..35: rope)
-          uint32_t h[8];
-          const uint32_t row = raw + raw_row_off(tok, L::kCopyS);
-          if ((mask >> tok) & 1ull) {
-            if constexpr (L::kNv) {
-              if (c16 < 32) {
-                const uint2 pl = ld_shared_v2(row + c16 * 8);
-                const uint32_t sc = ld_shared_u8(row + kScaleOff + c16);
-                const uint32_t s2h = e4m3x2_to_f16x2(static_cast<uint16_t>(sc | (sc << 8)));
-                uint32_t lo[4], hi[4];
-                e2m1x8_to_f16x8(pl.x, lo);
-                e2m1x8_to_f16x8(pl.y, hi);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  h[q] = hmul2_u32(lo[q], s2h);
-                  h[4 + q] = hmul2_u32(hi[q], s2h);
-                }
-              } else {
-                const uint4 v = ld_shared_v4(row + kRopeOff + (c16 - 32) * 16);
-                const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] & 0xFFFFu));
-                  h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
-                }
-              }
-            } else {
-              const uint4 v = ld_shared_v4(row + c16 * 16);
-              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                h[2 * q] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] & 0xFFFFu));
-                h[2 * q + 1] = e4m3x2_to_f16x2(static_cast<uint16_t>(w[q] >> 16));
-              }
-            }
-          } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) h[q] = 0u;
-          }
-          const uint32_t kb = static_cast<uint32_t>(c16 >> 2);
-          const uint32_t c0 = static_cast<uint32_t>((c16 & 3) * 2);
-          const uint32_t base = ktile + kb * 8192u;
-          st_shared_v4(base + sw128_off(tok, c0), h[0], h[1], h[2], h[3]);
-          st_shared_v4(base + sw128_off(tok, c0 + 1), h[4], h[5], h[6], h[7]);
+          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * sr);
+      const bool ok = (mask >> (row & 63)) & 1ull;
+      const uint32_t src = raw_base + sr * L::kStageS + raw_row_off(row & 63, L::kCopyS);
+#pragma unroll 1
+      for (int kb = 0; kb < kChunksPerTile; ++kb) {
+        const int q = i * kChunksPerTile + kb;
+        const int cs = q % kChunkSlots;
+        if (!warp_wait(bar(Ctl::kChunkEmpty, cs), ((q / kChunkSlots) & 1u) ^ 1u, abort_addr)) {
+          run = false;
+          break;
         }
-      } else {
-        // V^T tile [512 dims][64 tokens]: one item = 8 tokens x 16 dims. The
-        // transpose happens in registers: each converted f16x2 holds two dims
-        // of one token; prmt pairs the same dim of two tokens.
-        const uint32_t vtile = sbase + s2 * L::kVTile;
-        const int tg = dt & 7;   // token group (8 consecutive tokens)
-        const int j = dt >> 3;   // 16-dim group 0..31
-        if constexpr (L::kNv) {
-          uint32_t pw[8][2], scl[8];
+        uint32_t h[16];
+        if (!ok) {
 #pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            const int tok = tg * 8 + tt;
-            const uint32_t row = raw + raw_row_off(tok, L::kCopyO);
-            const bool ok = (mask >> tok) & 1ull;
-            const uint2 pl = ok ? ld_shared_v2(row + j * 8) : make_uint2(0u, 0u);
-            pw[tt][0] = pl.x;
-            pw[tt][1] = pl.y;
-            const uint32_t sc = ok ? ld_shared_u8(row + kScaleOff + j) : 0u;
-            scl[tt] = e4m3x2_to_f16x2(static_cast<uint16_t>(sc | (sc << 8)));
-          }
+          for (int x = 0; x < 16; ++x) h[x] = 0u;
+        } else if (L::kNv && kb < 8) {
+          const uint4 c = ld_shared_v4(src + 32 * kb + 16 * hf);
+          const uint32_t sc = ld_shared_u16(src + kScaleOff + 4 * kb + 2 * hf);
+          const uint32_t s0 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc & 0xFFu) * 0x0101u));
+          const uint32_t s1 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc >> 8) * 0x0101u));
+          const uint32_t w[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-          for (int wi = 0; wi < 2; ++wi) {
-            uint32_t hh[8][4];
+          for (int x = 0; x < 4; ++x) {
+            uint32_t f[4];
+            e2m1x8_to_f16x8(w[x], f);
+            const uint32_t sx = x < 2 ? s0 : s1;
 #pragma unroll
-            for (int tt = 0; tt < 8; ++tt) {
-              e2m1x8_to_f16x8(pw[tt][wi], hh[tt]);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) hh[tt][q] = hmul2_u32(hh[tt][q], scl[tt]);
-            }
-#pragma unroll
-            for (int bq = 0; bq < 4; ++bq) {
-              const uint32_t d0 = static_cast<uint32_t>(j * 16 + wi * 8 + 2 * bq);
-              st_shared_v4(vtile + sw128_off(d0, tg), prmt(hh[0][bq], hh[1][bq], 0x5410u),
-                           prmt(hh[2][bq], hh[3][bq], 0x5410u), prmt(hh[4][bq], hh[5][bq], 0x5410u),
-                           prmt(hh[6][bq], hh[7][bq], 0x5410u));
-              st_shared_v4(vtile + sw128_off(d0 + 1, tg), prmt(hh[0][bq], hh[1][bq], 0x7632u),
-                           prmt(hh[2][bq], hh[3][bq], 0x7632u), prmt(hh[4][bq], hh[5][bq], 0x7632u),
-                           prmt(hh[6][bq], hh[7][bq], 0x7632u));
-            }
+            for (int y = 0; y < 4; ++y) h[4 * x + y] = hmul2_u32(f[y], sx);
           }
         } else {
+          // E4M3 bytes: NVFP4 rope (row offset 288) or FP8 latent / rope (64 kb)
+          const uint32_t at = L::kNv ? kRopeOff + 32 * hf : 64 * kb + 32 * hf;
+          uint32_t lo[8], hi[8];
+          e4m3x16_to_f16(ld_shared_v4(src + at), lo);
+          e4m3x16_to_f16(ld_shared_v4(src + at + 16), hi);
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t ww[8][2];
+          for (int x = 0; x < 8; ++x) {
+            h[x] = lo[x];
+            h[8 + x] = hi[x];
+          }
+        }
+        const uint32_t dst = sbase + cs * L::kChunk;
 #pragma unroll
-            for (int tt = 0; tt < 8; ++tt) {
-              const int tok = tg * 8 + tt;
-              const uint32_t row = raw + raw_row_off(tok, L::kCopyO);
-              const bool ok = (mask >> tok) & 1ull;
-              const uint2 v = ok ? ld_shared_v2(row + j * 16 + half * 8) : make_uint2(0u, 0u);
-              ww[tt][0] = v.x;
-              ww[tt][1] = v.y;
-            }
+        for (int c = 0; c < 4; ++c)
+          st_shared_v4(dst + sw128_off(row, 4 * hf + c), h[4 * c], h[4 * c + 1], h[4 * c + 2],
+                       h[4 * c + 3]);
+        fence_proxy_async_cta();  // generic stores -> visible to the tensor core
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ctl::kChunkFull, cs));
+      }
+      __syncwarp();
+      if (lane == 0 && run) {
+        mbar_arrive(bar(Ctl::kRawEmpty, sa));
+        mbar_arrive(bar(Ctl::kRawEmpty, sb));
+      }
+    }
+  } else if (warp >= kDequantWarp0) {
+    // ------------------------------------------------ output CTA dequant: V^T tiles
+    // V^T [512 dims][64 rows]: one item = 8 rows x 16 dims; the transpose is
+    // done in registers (prmt pairs the same dim of two rows).
+    const int dt = tid - kDequantWarp0 * 32;
+    const int tg = dt & 7;  // row group (8 consecutive rows)
+    const int j = dt >> 3;  // 16-dim group 0..31
+    for (int u = 0; u < n_sub; ++u) {
+      const int s = u % L::kStagesO;
+      const uint32_t k = u / L::kStagesO;
+      const int s2 = u & 1;
+      const uint32_t k2 = u >> 1;
+      if (!warp_wait(bar(Ctl::kRawFull, s), k & 1u, abort_addr)) break;
+      if (!warp_wait(bar(Ctl::kVtEmpty, s2), (k2 & 1u) ^ 1u, abort_addr)) break;
+      const uint64_t mask =
+          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * s);
+      const uint32_t raw = raw_base + s * L::kStageO;
+      const uint32_t vtile = sbase + s2 * L::kVTile;
+      if constexpr (L::kNv) {
+        uint32_t pw[8][2], scl[8];
 #pragma unroll
-            for (int pi = 0; pi < 4; ++pi) {  // byte pair pi -> dims 2pi, 2pi+1 of this half
-              uint32_t f[8];
+        for (int tt = 0; tt < 8; ++tt) {
+          const int r = tg * 8 + tt;
+          const uint32_t rr = raw + raw_row_off(r, L::kCopyO);
+          const bool ok = (mask >> r) & 1ull;
+          const uint2 pl = ok ? ld_shared_v2(rr + j * 8) : make_uint2(0u, 0u);
+          pw[tt][0] = pl.x;
+          pw[tt][1] = pl.y;
+          const uint32_t sc = ok ? ld_shared_u8(rr + kScaleOff + j) : 0u;
+          scl[tt] = e4m3x2_to_f16x2(static_cast<uint16_t>(sc | (sc << 8)));
+        }
 #pragma unroll
-              for (int tt = 0; tt < 8; ++tt)
-                f[tt] = e4m3x2_to_f16x2(
-                    static_cast<uint16_t>((ww[tt][pi >> 1] >> (16 * (pi & 1))) & 0xFFFFu));
-              const uint32_t d0 = static_cast<uint32_t>(j * 16 + half * 8 + 2 * pi);
-              st_shared_v4(vtile + sw128_off(d0, tg), prmt(f[0], f[1], 0x5410u),
-                           prmt(f[2], f[3], 0x5410u), prmt(f[4], f[5], 0x5410u),
-                           prmt(f[6], f[7], 0x5410u));
-              st_shared_v4(vtile + sw128_off(d0 + 1, tg), prmt(f[0], f[1], 0x7632u),
-                           prmt(f[2], f[3], 0x7632u), prmt(f[4], f[5], 0x7632u),
-                           prmt(f[6], f[7], 0x7632u));
-            }
+        for (int wi = 0; wi < 2; ++wi) {
+          uint32_t hh[8][4];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            e2m1x8_to_f16x8(pw[tt][wi], hh[tt]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) hh[tt][q] = hmul2_u32(hh[tt][q], scl[tt]);
+          }
+#pragma unroll
+          for (int bq = 0; bq < 4; ++bq) {
+            const uint32_t d0 = static_cast<uint32_t>(j * 16 + wi * 8 + 2 * bq);
+            st_shared_v4(vtile + sw128_off(d0, tg), prmt(hh[0][bq], hh[1][bq], 0x5410u),
+                         prmt(hh[2][bq], hh[3][bq], 0x5410u), prmt(hh[4][bq], hh[5][bq], 0x5410u),
+                         prmt(hh[6][bq], hh[7][bq], 0x5410u));
+            st_shared_v4(vtile + sw128_off(d0 + 1, tg), prmt(hh[0][bq], hh[1][bq], 0x7632u),
+                         prmt(hh[2][bq], hh[3][bq], 0x7632u), prmt(hh[4][bq], hh[5][bq], 0x7632u),
+                         prmt(hh[6][bq], hh[7][bq], 0x7632u));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t ww[8][2];
+#pragma unroll
+          for (int tt = 0; tt < 8; ++tt) {
+            const int r = tg * 8 + tt;
+            const uint32_t rr = raw + raw_row_off(r, L::kCopyO);
+            const bool ok = (mask >> r) & 1ull;
+            const uint2 v = ok ? ld_shared_v2(rr + j * 16 + half * 8) : make_uint2(0u, 0u);
+            ww[tt][0] = v.x;
+            ww[tt][1] = v.y;
+          }
+#pragma unroll
+          for (int pi = 0; pi < 4; ++pi) {  // byte pair pi -> dims 2pi, 2pi+1 of this half
+            uint32_t f[8];
+#pragma unroll
+            for (int tt = 0; tt < 8; ++tt)
+              f[tt] = e4m3x2_to_f16x2(
+                  static_cast<uint16_t>((ww[tt][pi >> 1] >> (16 * (pi & 1))) & 0xFFFFu));
+            const uint32_t d0 = static_cast<uint32_t>(j * 16 + half * 8 + 2 * pi);
+            st_shared_v4(vtile + sw128_off(d0, tg), prmt(f[0], f[1], 0x5410u),
+                         prmt(f[2], f[3], 0x5410u), prmt(f[4], f[5], 0x5410u),
+                         prmt(f[6], f[7], 0x5410u));
+            st_shared_v4(vtile + sw128_off(d0 + 1, tg), prmt(f[0], f[1], 0x7632u),
+                         prmt(f[2], f[3], 0x7632u), prmt(f[4], f[5], 0x7632u),
+                         prmt(f[6], f[7], 0x7632u));
           }
         }
       }
-      fence_proxy_async_cta();  // generic-proxy stores -> visible to the tensor core
+      fence_proxy_async_cta();
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar(Ctl::kTileFull, s2));
+        mbar_arrive(bar(Ctl::kVtFull, s2));
         mbar_arrive(bar(Ctl::kRawEmpty, s));
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---------------------------------------------- MMA issue (one thread)
+    // ------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
-      int issued = 0;
+      uint32_t last_bar = 0, last_parity = 0;
+      bool issued = false;
       if (rank == 0) {
         if (wait_bar(bar(Ctl::kQReady, 0), 0, abort_addr)) {
-          for (int i = 0; i < n_tiles; ++i) {
+          const uint64_t qrope = sw128_desc(sbase + L::kQRope);
+          bool run = true;
+          for (int i = 0; i < n_tiles && run; ++i) {
             const int s2 = i & 1;
             const uint32_t k2 = i >> 1;
-            if (!wait_bar(bar(Ctl::kTileFull, s2), k2 & 1u, abort_addr)) break;
             if (!wait_bar(bar(Ctl::kSEmpty, s2), (k2 & 1u) ^ 1u, abort_addr)) break;
-            tc_fence_after();
-            const uint32_t ktile = sbase + s2 * L::kKTile;
-            const uint32_t dcol = tmem + kSCol + 64u * s2;
-#pragma unroll 4
-            for (int kk = 0; kk < 36; ++kk) {
-              const uint64_t bdesc = sw128_desc(ktile + (kk >> 2) * 8192u + (kk & 3) * 32u);
-              mma_ts(dcol, tmem + kQCol + 8u * kk, bdesc, kIdescQK, kk > 0 ? 1u : 0u);
+            const uint32_t dcol = tmem + kSCol + 128u * s2;
+            for (int kb = 0; kb < kChunksPerTile; ++kb) {
+              const int q = i * kChunksPerTile + kb;
+              const int cs = q % kChunkSlots;
+              if (!wait_bar(bar(Ctl::kChunkFull, cs), (q / kChunkSlots) & 1u, abort_addr)) {
+                run = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t chunk = sbase + cs * L::kChunk;
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk) {
+                const uint64_t bdesc = sw128_desc(chunk + 32u * kk);
+                if (kb < 8)
+                  mma_ts(dcol, tmem + 32u * kb + 8u * kk, bdesc, kIdescQK, (kb | kk) != 0);
+                else
+                  mma_ss(dcol, qrope + 2u * kk, bdesc, kIdescQK, 1u);
+              }
+              mma_commit(bar(Ctl::kChunkEmpty, cs));
+              last_bar = bar(Ctl::kChunkEmpty, cs);
+              last_parity = (q / kChunkSlots) & 1u;
+              issued = true;
             }
-            mma_commit(bar(Ctl::kTileEmpty, s2));
-            mma_commit(bar(Ctl::kSFull, s2));
-            issued = i + 1;
+            if (run) mma_commit(bar(Ctl::kSFull, s2));
           }
         }
       } else {
         uint32_t n_corr = 0;
-        for (int i = 0; i < n_tiles; ++i) {
-          const int s2 = i & 1;
-          const uint32_t k2 = i >> 1;
-          if (!wait_bar(bar(Ctl::kTileFull, s2), k2 & 1u, abort_addr)) break;
+        for (int u = 0; u < n_sub; ++u) {
+          const int s2 = u & 1;
+          const uint32_t k2 = u >> 1;
+          if (!wait_bar(bar(Ctl::kVtFull, s2), k2 & 1u, abort_addr)) break;
           if (!wait_bar(bar(Ctl::kPFull, s2), k2 & 1u, abort_addr)) break;
-          const uint4 fl = ld_shared_v4(ctl + Ctl::kFlags + 16 * s2);
+          const uint4 fl = ld_shared_v4(ctl + Ctl::kAF + s2 * kAFBytes + 512);
           if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
             if (!wait_bar(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr)) break;
             ++n_corr;
           }
           tc_fence_after();
-          fence_proxy_async_cta();
           const uint32_t vtile = sbase + s2 * L::kVTile;
           const uint32_t ptile = sbase + L::kP + s2 * L::kPTile;
 #pragma unroll
@@ -609,158 +769,220 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int nh = 0; nh < 2; ++nh) {
               const uint64_t bdesc = sw128_desc(vtile + nh * 32768u + kk * 32u);
-              mma_ss(tmem + 256u * nh, adesc, bdesc, kIdescPV, (i > 0 || kk > 0) ? 1u : 0u);
+              mma_ss(tmem + 256u * nh, adesc, bdesc, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          mma_commit(bar(Ctl::kTileEmpty, s2));
+          mma_commit(bar(Ctl::kVtEmpty, s2));
           mma_commit(bar(Ctl::kPvDone, s2));
-          issued = i + 1;
+          last_bar = bar(Ctl::kVtEmpty, s2);
+          last_parity = k2 & 1u;
+          issued = true;
         }
       }
-      if (issued > 0) {  // the last commit completes once every MMA issued here has
-        const int last = issued - 1;
-        drain_bar(bar(Ctl::kTileEmpty, last & 1), (static_cast<uint32_t>(last) >> 1) & 1u);
-      }
+      if (issued) drain_bar(last_bar, last_parity);  // every issued MMA has completed
     }
   } else if (rank == 0) {
-    // ---------------------------------------------- score CTA: Q -> TMEM, then softmax
+    // ------------------------------------------------ score CTA: Q setup, then softmax
     const int h = warp * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    bool ok;
     {
-      const bool live = h < p.num_heads;
-      const int64_t qh = static_cast<int64_t>(t) * p.num_heads + h;
+      // Q (bf16) of this token arrives by two bulk copies over the still
+      // unused buffers; each thread converts its head's row to FP16 (scales
+      // folded in): the latent part into TMEM, the rope part into the
+      // swizzled shared-memory operand.
+      const uint32_t qbar = bar(Ctl::kQFull, 0);
+      const uint32_t lat_bytes = static_cast<uint32_t>(p.num_heads) * (kLatent * 2);
+      const uint32_t rope_at = sbase + L::kQStage + 128u * kLatent * 2;
+      if (tid == 0) {
+        mbar_arrive_tx(qbar, lat_bytes + static_cast<uint32_t>(p.num_heads) * (kRope * 2));
+        bulk_g2s(sbase + L::kQStage, p.q_lat + static_cast<int64_t>(t) * p.num_heads * kLatent,
+                 lat_bytes, qbar);
+        bulk_g2s(rope_at, p.q_rope + static_cast<int64_t>(t) * p.num_heads * kRope,
+                 static_cast<uint32_t>(p.num_heads) * (kRope * 2), qbar);
+      }
+      ok = group_and(wait_bar(qbar, 0, abort_addr));
+      const bool live = ok && h < p.num_heads;
 #pragma unroll 1
-      for (int c = 0; c < 9; ++c) {
+      for (int c = 0; c < 8; ++c) {
         uint32_t r[32];
-        const float m = c < 8 ? p.q_lat_mult : p.q_rope_mult;
+        const uint32_t src = sbase + L::kQStage + h * (kLatent * 2) + c * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          uint4 x = make_uint4(0u, 0u, 0u, 0u);
-          if (live)
-            x = c < 8 ? ld_nc_v4(p.q_lat + qh * kLatent + c * 64 + v * 8)
-                      : ld_nc_v4(p.q_rope + qh * kRope + v * 8);
-          r[4 * v + 0] = pack_f16x2(bf16_lo(x.x) * m, bf16_hi(x.x) * m);
-          r[4 * v + 1] = pack_f16x2(bf16_lo(x.y) * m, bf16_hi(x.y) * m);
-          r[4 * v + 2] = pack_f16x2(bf16_lo(x.z) * m, bf16_hi(x.z) * m);
-          r[4 * v + 3] = pack_f16x2(bf16_lo(x.w) * m, bf16_hi(x.w) * m);
+          const uint4 x = bf16x8_to_f16x8(
+              live ? ld_shared_v4(src + v * 16) : make_uint4(0u, 0u, 0u, 0u), p.q_lat_mult);
+          r[4 * v] = x.x;
+          r[4 * v + 1] = x.y;
+          r[4 * v + 2] = x.z;
+          r[4 * v + 3] = x.w;
         }
-        tmem_st32(tmem + lane_base + kQCol + 32u * c, r);
+        tmem_st32(tmem + lane_base + 32u * c, r);
       }
+      uint4 qr[8];
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        qr[v] = bf16x8_to_f16x8(live ? ld_shared_v4(rope_at + h * (kRope * 2) + v * 16)
+                                     : make_uint4(0u, 0u, 0u, 0u),
+                                p.q_rope_mult);
       tmem_st_wait();
+      group_sync();  // every staged row has been read: the rope operand may overwrite it
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        st_shared_v4(sbase + L::kQRope + sw128_off(h, v), qr[v].x, qr[v].y, qr[v].z, qr[v].w);
+      fence_proxy_async_cta();
       tc_fence_before();
       mbar_arrive(bar(Ctl::kQReady, 0));
     }
     const uint32_t peer_p = map_rank(sbase + L::kP, peer);
     const uint32_t peer_ctl = map_rank(ctl, peer);
+    const float c = p.score_scale;
     float m_ref = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
+    for (int i = 0; i < n_tiles && ok; ++i) {
       const int s2 = i & 1;
       const uint32_t k2 = i >> 1;
-      if (!warp_wait(bar(Ctl::kSFull, s2), k2 & 1u, abort_addr)) { ok = false; break; }
+      ok = group_and(wait_bar(bar(Ctl::kSFull, s2), k2 & 1u, abort_addr));
+      if (!ok) break;
       tc_fence_after();
-      const uint64_t mask =
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (i & 7));
-      uint32_t sa[32], sb[32];
-      tmem_ld32(tmem + lane_base + kSCol + 64u * s2, sa);
-      tmem_ld32(tmem + lane_base + kSCol + 64u * s2 + 32u, sb);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(bar(Ctl::kSEmpty, s2));
-      float mx = -INFINITY;
+      uint64_t masks[2];
+      masks[0] = *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing +
+                                                        8 * ((2 * i) & 15));
+      masks[1] = *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing +
+                                                        8 * ((2 * i + 1) & 15));
+#pragma unroll 1
+      for (int jj = 0; jj < 2; ++jj) {
+        const int u = 2 * i + jj;
+        const uint64_t mask = masks[jj];
+        uint32_t sa[32], sb[32];
+        tmem_ld32(tmem + lane_base + kSCol + 128u * s2 + 64u * jj, sa);
+        tmem_ld32(tmem + lane_base + kSCol + 128u * s2 + 64u * jj + 32u, sb);
+        tmem_ld_wait();
+        if (jj == 1) {
+          tc_fence_before();
+          mbar_arrive(bar(Ctl::kSEmpty, s2));
+        }
+        // raw max over the valid rows (the scale c > 0 is applied once after)
+        float mx = -INFINITY;
+        if (mask == ~0ull) {
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const float v0 = ((mask >> q) & 1ull) ? __uint_as_float(sa[q]) * p.score_scale : -INFINITY;
-        const float v1 =
-            ((mask >> (32 + q)) & 1ull) ? __uint_as_float(sb[q]) * p.score_scale : -INFINITY;
-        sa[q] = __float_as_uint(v0);
-        sb[q] = __float_as_uint(v1);
-        mx = fmaxf(mx, fmaxf(v0, v1));
-      }
-      float alpha = 1.f;
-      bool resc = false;
-      if (mx > m_ref + kTau) {  // also the first valid score (m_ref = -inf)
-        alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - mx);
-        m_ref = mx;
-        l *= alpha;
-        resc = true;
-      }
-      uint32_t pk[32];
-      float sum = 0.f;
+          for (int q = 0; q < 32; ++q)
+            mx = fmaxf(mx, fmaxf(__uint_as_float(sa[q]), __uint_as_float(sb[q])));
+        } else {
 #pragma unroll
-      for (int q = 0; q < 32; ++q) {
-        const uint32_t* src = q < 16 ? sa : sb;
-        const int qq = (q & 15) * 2;
-        const float p0 = m_ref == -INFINITY ? 0.f : ex2(__uint_as_float(src[qq]) - m_ref);
-        const float p1 = m_ref == -INFINITY ? 0.f : ex2(__uint_as_float(src[qq + 1]) - m_ref);
-        pk[q] = pack_f16x2(p0, p1);
-        sum += f16_bits_to_f32(static_cast<uint16_t>(pk[q] & 0xFFFFu)) +
-               f16_bits_to_f32(static_cast<uint16_t>(pk[q] >> 16));
-      }
-      l += sum;
-      // P buffer s2 of the peer is free once its PV of tile i-2 completed
-      if (!warp_wait(bar(Ctl::kPEmpty, s2), (k2 & 1u) ^ 1u, abort_addr)) { ok = false; break; }
-      const uint32_t prow = peer_p + s2 * L::kPTile;
+          for (int q = 0; q < 32; ++q) {
+            const float v0 = ((mask >> q) & 1ull) ? __uint_as_float(sa[q]) : -INFINITY;
+            const float v1 = ((mask >> (32 + q)) & 1ull) ? __uint_as_float(sb[q]) : -INFINITY;
+            sa[q] = __float_as_uint(v0);
+            sb[q] = __float_as_uint(v1);
+            mx = fmaxf(mx, fmaxf(v0, v1));
+          }
+        }
+        const float mxs = mx * c;
+        float alpha = 1.f;
+        bool resc = false;
+        if (mxs > m_ref + kTau) {  // also the first valid score (m_ref = -inf)
+          alpha = m_ref == -INFINITY ? 0.f : ex2(m_ref - mxs);
+          m_ref = mxs;
+          l *= alpha;
+          resc = true;
+        }
+        const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
+        const bool none = m_ref == -INFINITY;
+        uint32_t pk[32];
+        float sum = 0.f;
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
-        st_cluster_v4(prow + sw128_off(h, c), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2],
-                      pk[4 * c + 3]);
-      st_cluster_u32(peer_ctl + Ctl::kAlpha + 4 * (s2 * 128 + h), __float_as_uint(alpha));
-      const bool warp_resc = __any_sync(0xffffffffu, resc && i > 0);
-      if (lane == 0)
-        st_cluster_u32(peer_ctl + Ctl::kFlags + 16 * s2 + 4 * warp, warp_resc ? 1u : 0u);
-      fence_proxy_async_cluster();
-      mbar_arrive_cluster(peer_ctl + Ctl::kPFull + 8 * s2);
+        for (int q = 0; q < 32; ++q) {
+          const uint32_t* src = q < 16 ? sa : sb;
+          const int qq = (q & 15) * 2;
+          // masked rows hold -inf: fma gives -inf, ex2 gives 0
+          const float p0 = none ? 0.f : ex2(fmaf(__uint_as_float(src[qq]), c, neg_m));
+          const float p1 = none ? 0.f : ex2(fmaf(__uint_as_float(src[qq + 1]), c, neg_m));
+          pk[q] = pack_f16x2(p0, p1);
+          sum += p0 + p1;
+        }
+        l += sum;
+        // stage P + rescale factor + flags; slot u & 1 of the staging area
+        const int st = u & 1;
+        const uint32_t stage = sbase + L::kPStage + st * L::kPStageStride;
+        if (tid == 0) bulk_wait_read<1>();  // the copy that last used this slot has read it
+        group_sync();
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc)
+          st_shared_v4(stage + sw128_off(h, cc), pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2],
+                       pk[4 * cc + 3]);
+        st_shared_u32(stage + 16384 + 4 * h, __float_as_uint(alpha));
+        const bool warp_resc = __any_sync(0xffffffffu, resc && u > 0);
+        if (lane == 0) st_shared_u32(stage + 16384 + 512 + 4 * warp, warp_resc ? 1u : 0u);
+        fence_proxy_async_cta();  // generic stores -> visible to the bulk copy
+        bool sent = true;
+        if (tid == 0) {
+          // the peer's P buffer st is free once its P V of sub-tile u-2 completed
+          sent = wait_bar(bar(Ctl::kPEmpty, st), ((u >> 1) & 1u) ^ 1u, abort_addr);
+        }
+        ok = group_and(sent);
+        if (!ok) break;
+        if (tid == 0) {
+          const uint32_t pbar = peer_ctl + Ctl::kPFull + 8 * st;
+          mbar_arrive_tx_cluster(pbar, 16384 + kAFBytes);
+          bulk_s2s(peer_p + st * L::kPTile, stage, 16384, pbar);
+          bulk_s2s(peer_ctl + Ctl::kAF + st * kAFBytes, stage + 16384, kAFBytes, pbar);
+          bulk_commit();
+        }
+      }
     }
+    if (tid == 0) bulk_wait_read<0>();  // this CTA's staging is read before it exits
     if (ok) {
       st_cluster_u32(peer_ctl + Ctl::kFinalM + 4 * h, __float_as_uint(m_ref));
       st_cluster_u32(peer_ctl + Ctl::kFinalL + 4 * h, __float_as_uint(l));
       mbar_arrive_cluster(peer_ctl + Ctl::kStats);
     }
   } else {
-    // ---------------------------------------------- output CTA: corrections + epilogue
+    // ------------------------------------------------ output CTA: corrections + epilogue
     const int h = warp * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t peer_ctl = map_rank(ctl, peer);
-    uint32_t n_corr = 0;
     bool ok = true;
-    for (int i = 0; i < n_tiles; ++i) {
-      const int s2 = i & 1;
-      const uint32_t k2 = i >> 1;
-      if (!warp_wait(bar(Ctl::kPvDone, s2), k2 & 1u, abort_addr)) { ok = false; break; }
+    for (int u = 0; u < n_sub; ++u) {
+      const int s2 = u & 1;
+      const uint32_t k2 = u >> 1;
+      if (!warp_wait(bar(Ctl::kPvDone, s2), k2 & 1u, abort_addr)) {
+        ok = false;
+        break;
+      }
       tc_fence_after();
-      // every correction thread read this slot's flags/alpha already (tile i, in
-      // the previous iteration): the score CTA may now refill the slot
+      // this thread has read buffer s2's flags and factor (for sub-tile u, in the
+      // previous iteration): the score CTA may refill it
       mbar_arrive_cluster(peer_ctl + Ctl::kPEmpty + 8 * s2);
-      if (i + 1 < n_tiles) {
-        const int n2 = (i + 1) & 1;
-        const uint32_t nk2 = (i + 1) >> 1;
-        if (!warp_wait(bar(Ctl::kPFull, n2), nk2 & 1u, abort_addr)) { ok = false; break; }
-        const uint4 fl = ld_shared_v4(ctl + Ctl::kFlags + 16 * n2);
+      if (u + 1 < n_sub) {
+        const int n2 = (u + 1) & 1;
+        const uint32_t nk2 = (u + 1) >> 1;
+        if (!warp_wait(bar(Ctl::kPFull, n2), nk2 & 1u, abort_addr)) {
+          ok = false;
+          break;
+        }
+        const uint32_t af = ctl + Ctl::kAF + n2 * kAFBytes;
+        const uint4 fl = ld_shared_v4(af + 512);
         if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
-          const float alpha =
-              *reinterpret_cast<volatile float*>(smem + L::kCtl + Ctl::kAlpha + 4 * (n2 * 128 + h));
+          const float alpha = __uint_as_float(ld_shared_u32(af + 4 * h));
 #pragma unroll 1
-          for (int c = 0; c < 16; ++c) {
+          for (int cc = 0; cc < 16; ++cc) {
             uint32_t r[32];
-            tmem_ld32(tmem + lane_base + 32u * c, r);
+            tmem_ld32(tmem + lane_base + 32u * cc, r);
             tmem_ld_wait();
 #pragma unroll
             for (int q = 0; q < 32; ++q) r[q] = __float_as_uint(__uint_as_float(r[q]) * alpha);
-            tmem_st32(tmem + lane_base + 32u * c, r);
+            tmem_st32(tmem + lane_base + 32u * cc, r);
           }
           tmem_st_wait();
           tc_fence_before();
           mbar_arrive(bar(Ctl::kOCorr, 0));
-          ++n_corr;
         }
       }
     }
     float m_fin = NAN, l_fin = 0.f;
     ok = __all_sync(0xffffffffu, ok);
     if (ok && warp_wait(bar(Ctl::kStats, 0), 0, abort_addr)) {
-      m_fin = *reinterpret_cast<volatile float*>(smem + L::kCtl + Ctl::kFinalM + 4 * h);
-      l_fin = *reinterpret_cast<volatile float*>(smem + L::kCtl + Ctl::kFinalL + 4 * h);
+      m_fin = __uint_as_float(ld_shared_u32(ctl + Ctl::kFinalM + 4 * h));
+      l_fin = __uint_as_float(ld_shared_u32(ctl + Ctl::kFinalL + 4 * h));
     } else {
       ok = false;
     }
@@ -774,10 +996,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float sc = single ? inv * p.out_mult : inv;
       const int64_t part = (static_cast<int64_t>(t) * p.num_splits + split) * p.num_heads + h;
 #pragma unroll 1
-      for (int c = 0; c < 16; ++c) {
+      for (int cc = 0; cc < 16; ++cc) {
         uint32_t r[32];
         if (ok) {
-          tmem_ld32(tmem + lane_base + 32u * c, r);
+          tmem_ld32(tmem + lane_base + 32u * cc, r);
           tmem_ld_wait();
         } else {
 #pragma unroll
@@ -789,7 +1011,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(r[q]) * sc;
         if (single && !p.out_fp32) {
           uint4* dst =
-              reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qh * kLatent + c * 32);
+              reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qh * kLatent + cc * 32);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
@@ -797,8 +1019,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                 pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
                                 pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
         } else {
-          float* dst = single ? static_cast<float*>(p.out) + qh * kLatent + c * 32
-                              : p.ws + part * kLatent + c * 32;
+          float* dst = single ? static_cast<float*>(p.out) + qh * kLatent + cc * 32
+                              : p.ws + part * kLatent + cc * 32;
 #pragma unroll
           for (int q = 0; q < 8; ++q)
             reinterpret_cast<float4*>(dst)[q] =

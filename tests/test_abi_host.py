@@ -64,10 +64,11 @@ def test_workspace_size_host_logic(lib):
     # one split needs nothing; s splits need num_q * s * H * 513 floats
     assert lib.sparse_mla_decode_workspace_size(4, 16, 2048, 1) == 0
     assert lib.sparse_mla_decode_workspace_size(4, 16, 2048, 4) == 4 * 4 * 16 * 513 * 4
-    # splits are clamped to the number of 64-slot tiles and never left empty
-    assert lib.sparse_mla_decode_workspace_size(2, 8, 100, 8) == 2 * 2 * 8 * 513 * 4
-    assert lib.sparse_mla_decode_workspace_size(1, 8, 640, 4) == 1 * 4 * 8 * 513 * 4  # 3,3,3,1
-    assert lib.sparse_mla_decode_workspace_size(1, 8, 576, 4) == 1 * 3 * 8 * 513 * 4  # 3,3,3
+    # splits are clamped to the number of 128-slot tiles and never left empty
+    assert lib.sparse_mla_decode_workspace_size(2, 8, 200, 8) == 2 * 2 * 8 * 513 * 4
+    assert lib.sparse_mla_decode_workspace_size(2, 8, 100, 8) == 0  # one tile: one split
+    assert lib.sparse_mla_decode_workspace_size(1, 8, 1280, 4) == 1 * 4 * 8 * 513 * 4  # 3,3,3,1
+    assert lib.sparse_mla_decode_workspace_size(1, 8, 1152, 4) == 1 * 3 * 8 * 513 * 4  # 3,3,3
 
 
 # ------------------------------------------------------------ validation
