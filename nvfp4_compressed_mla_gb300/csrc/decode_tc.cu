@@ -50,11 +50,13 @@ namespace nvfp4_mla {
 namespace {
 
 constexpr int kSub = 64;             // rows per gather stage / P sub-tile
-constexpr int kWarps = 14;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 6;
+constexpr int kCopyWarp0 = 6;        // warps 6-7: gather copies
+constexpr int kCopyThreads = 64;
+constexpr int kDequantWarp0 = 8;     // warps 8-15: dequant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;      // score CTA: S buffers at columns 256 and 384
 constexpr int kChunkSlots = 4;
@@ -62,7 +64,8 @@ constexpr int kChunksPerTile = 9;    // 8 latent + 1 rope
 constexpr float kTau = 8.0f;         // lazy rescale threshold (log2 units)
 constexpr long long kWaitCycles = 1ll << 31;
 constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t kIdescPV = (1u << 4) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
+// P V: B (= V, rows x dims) is read MN-major (dims contiguous): bit 16
+constexpr uint32_t kIdescPV = (1u << 4) | (1u << 16) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kAFBytes = 528;   // per P buffer: 128 fp32 rescale factors + 4 warp flags
 
 template <int kFmt>
@@ -76,36 +79,42 @@ struct TcLayout {
   static constexpr int kStageO = kSub * kCopyO + 8 * kPad;
   static constexpr int kStagesS = kNv ? 4 : 3;
   static constexpr int kStagesO = kNv ? 3 : 2;
+  static constexpr int kOffsSlots = kNv ? 8 : 6;  // resolved row offsets, 64 per slot
+  static constexpr int kOffsBytes = kOffsSlots * (kSub * 4 + 8);
   // score CTA
   static constexpr int kChunk = 16384;            // 128 rows x 64 dims FP16
   static constexpr int kQRope = kChunkSlots * kChunk;
   static constexpr int kPStage = kQRope + 16384;  // 2 x [P 16 KB][rescale + flags]
   static constexpr int kPStageStride = 17408;
   static constexpr int kRawS = kPStage + 2 * kPStageStride;
-  static constexpr int kEndS = kRawS + kStagesS * kStageS;
+  static constexpr int kOffsS = kRawS + kStagesS * kStageS;
+  static constexpr int kEndS = kOffsS + kOffsBytes;
   static constexpr int kQStage = 0;               // start-up: Q (bf16) staged over the above
   static constexpr int kQStageBytes = 128 * (kLatent + kRope) * 2;
   // output CTA
-  static constexpr int kVTile = 64 * 1024;        // 512 dims x 64 rows FP16
+  static constexpr int kVSlot = 32 * 1024;        // 32 rows x 512 dims FP16 (MN-major)
+  static constexpr int kVSlots = 3;
   static constexpr int kPTile = 16 * 1024;        // 128 heads x 64 rows FP16
-  static constexpr int kP = 2 * kVTile;
+  static constexpr int kP = kVSlots * kVSlot;
   static constexpr int kRawO = kP + 2 * kPTile;
-  static constexpr int kEndO = kRawO + kStagesO * kStageO;
+  static constexpr int kOffsO = kRawO + kStagesO * kStageO;
+  static constexpr int kEndO = kOffsO + kOffsBytes;
   static constexpr int kCtl = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
-  static constexpr int kCtlBytes = 2560;
+  static constexpr int kCtlBytes = 2768;
   static constexpr int kBytes = kCtl + kCtlBytes;
   static_assert(kBytes <= 232448, "shared memory budget");
-  static_assert(kQStageBytes <= kEndS, "Q staging fits the score CTA's buffers");
-  static_assert(kStageS % 16 == 0 && kStageO % 16 == 0, "bulk copy alignment");
+  static_assert(kQStageBytes <= kRawS + kStagesS * kStageS, "Q staging fits the score CTA's buffers");
+  static_assert(kStageS % 16 == 0 && kStageO % 16 == 0 && kP % 1024 == 0, "alignment");
 };
 
 // control block: same offset in both CTAs of the cluster
 struct Ctl {
   static constexpr int kRawFull = 0, kRawEmpty = 32, kChunkFull = 64, kChunkEmpty = 96,
-                       kVtFull = 128, kVtEmpty = 144, kSFull = 160, kSEmpty = 176, kPFull = 192,
-                       kPEmpty = 208, kPvDone = 224, kOCorr = 240, kStats = 248, kQReady = 256,
-                       kQFull = 264, kTmem = 272, kAbort = 276, kStageMask = 280,
-                       kMaskRing = 312, kAF = 448, kFinalM = 1504, kFinalL = 2016, kEnd = 2528;
+                       kVtFull = 128, kVtEmpty = 152, kSFull = 176, kSEmpty = 192, kPFull = 208,
+                       kPEmpty = 224, kPvDone = 240, kOCorr = 256, kStats = 264, kQReady = 272,
+                       kQFull = 280, kOffsFull = 288, kOffsEmpty = 352, kTmem = 416,
+                       kAbort = 420, kMaskRing = 424, kAF = 688, kFinalM = 1744, kFinalL = 2256,
+                       kEnd = 2768;
 };
 static_assert(Ctl::kEnd <= TcLayout<NVFP4_MLA_ROW_NVFP4_352>::kCtlBytes, "control block");
 static_assert(Ctl::kAF + 2 * kAFBytes <= Ctl::kFinalM, "rescale/flag slots");
@@ -199,11 +208,6 @@ __device__ __forceinline__ uint32_t ld_shared_u8(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
-}
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
 }
 
 // tcgen05
@@ -311,11 +315,6 @@ template <int kPending>
 __device__ __forceinline__ void bulk_wait_read() {
   asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
 }
-__device__ __forceinline__ uint32_t ld_shared_u16(uint32_t addr) {
-  uint32_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
-  return v;
-}
 // Barrier 1 over the 128 threads of warps 0-3, returning the AND of `v` over them.
 __device__ __forceinline__ bool group_and(bool v) {
   uint32_t r;
@@ -333,6 +332,15 @@ __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" :
 // 1024 bytes apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
   return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// The same for an MN-major operand whose 64-element blocks along N are 4096
+// bytes apart (leading byte offset) and whose 8-row groups along K are 1024
+// bytes apart (stride byte offset).
+__device__ __forceinline__ uint64_t sw128_desc_mn(uint32_t addr) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) | (static_cast<uint64_t>(4096 >> 4) << 16) |
          (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
          (static_cast<uint64_t>(2) << 61);
 }
@@ -418,16 +426,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(bar(Ctl::kRawFull, s), 32);
+      mbar_init(bar(Ctl::kRawFull, s), kCopyThreads);  // one cp.async arrival per copy thread
       mbar_init(bar(Ctl::kRawEmpty, s), 8);
+    }
+    for (int s = 0; s < L::kOffsSlots; ++s) {
+      mbar_init(bar(Ctl::kOffsFull, s), 1);
+      mbar_init(bar(Ctl::kOffsEmpty, s), kCopyThreads / 32);
     }
     for (int s = 0; s < kChunkSlots; ++s) {
       mbar_init(bar(Ctl::kChunkFull, s), 8);
       mbar_init(bar(Ctl::kChunkEmpty, s), 1);
     }
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < L::kVSlots; ++s) {
       mbar_init(bar(Ctl::kVtFull, s), 8);
       mbar_init(bar(Ctl::kVtEmpty, s), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(bar(Ctl::kSFull, s), 1);
       mbar_init(bar(Ctl::kSEmpty, s), 128);
       mbar_init(bar(Ctl::kPFull, s), 1);
@@ -455,12 +469,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t raw_base = sbase + (rank == 0 ? L::kRawS : L::kRawO);
   const uint32_t stage_bytes = rank == 0 ? L::kStageS : L::kStageO;
 
+  const uint32_t offs_base = sbase + (rank == 0 ? L::kOffsS : L::kOffsO);
+  auto offs_row = [&](int slot) { return offs_base + slot * (kSub * 4); };
+  auto offs_mask = [&](int slot) { return offs_base + L::kOffsSlots * (kSub * 4) + 8 * slot; };
+
+  // Copies of stage u (issued by the copy warps): consecutive threads
+  // take consecutive 16-byte pieces of the stage's rows, so a warp's copy
+  // instruction reads whole rows instead of 32 scattered pieces. The stage's
+  // barrier counts one arrival per thread, fired when its copies have landed.
+  auto issue_stage = [&](int u, int dt) -> bool {
+    const int os = u % L::kOffsSlots;
+    const int s = u % stages;
+    if (!warp_wait(bar(Ctl::kOffsFull, os), (u / L::kOffsSlots) & 1u, abort_addr)) return false;
+    if (!warp_wait(bar(Ctl::kRawEmpty, s), ((u / stages) & 1u) ^ 1u, abort_addr)) return false;
+    const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + (offs_mask(os) - sbase));
+    const int chunks = copy / 16;
+    const uint32_t dst = raw_base + s * stage_bytes;
+    for (int c = dt; c < kSub * chunks; c += kCopyThreads) {
+      const int r = c / chunks;
+      const int q = c - r * chunks;
+      if ((mask >> r) & 1ull) {
+        const uint64_t src16 = ld_shared_u32(offs_row(os) + 4 * r);
+        cp_async16(dst + raw_row_off(r, copy) + 16 * q, p.cache + (src16 << 4) + 16 * q);
+      }
+    }
+    cp_async_arrive_noinc(bar(Ctl::kRawFull, s));
+    __syncwarp();
+    if ((tid & 31) == 0) mbar_arrive(bar(Ctl::kOffsEmpty, os));
+    return true;
+  };
+
   if (warp == kProducerWarp) {
-    // ------------------------------------------------ gather: slots -> rows -> stages
-    // Index and block-table loads are dependent global loads. They run two
-    // stages ahead of the copies through a register ring that is indexed by
-    // compile-time slots (the loop is unrolled by the ring length), so no
-    // register hand-off waits on a load still in flight.
+    // ------------------------------------------------ resolve: slots -> row offsets
+    // Index and block-table loads are dependent global loads; four stages are
+    // resolved per batch with all their loads in flight together, and the
+    // next batch's index loads overlap this batch's block-table loads.
     const bool seq_ok = b >= 0 && b < p.num_seqs;
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(seq_ok ? b : 0) * p.max_blocks;
     auto load_pos = [&](int u, int32_t (&pos)[2]) {
@@ -485,41 +528,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
     };
-    const bool go = rank != 0 || warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
-    int32_t posr[6][2];
-    int64_t pgr[3][2];
+    int32_t posa[4][2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) load_pos(u, posr[u]);
-    load_page(posr[0], pgr[0]);
-    load_page(posr[1], pgr[1]);
-    bool stop = !go;
-    for (int u0 = 0; u0 < n_sub && !stop; u0 += 6) {
+    for (int k = 0; k < 4; ++k) load_pos(k, posa[k]);
+    bool stop = false;
+    for (int u0 = 0; u0 < n_sub && !stop; u0 += 4) {
+      int64_t pg[4][2];
+      int32_t posb[4][2];
 #pragma unroll
-      for (int du = 0; du < 6; ++du) {
-        const int u = u0 + du;
-        if (u >= n_sub) {
+      for (int k = 0; k < 4; ++k) load_page(posa[k], pg[k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) load_pos(u0 + 4 + k, posb[k]);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const int u = u0 + k;
+        if (u >= n_sub) break;
+        const int os = u % L::kOffsSlots;
+        if (!warp_wait(bar(Ctl::kOffsEmpty, os), ((u / L::kOffsSlots) & 1u) ^ 1u, abort_addr)) {
           stop = true;
           break;
         }
-        load_pos(u + 4, posr[(du + 4) % 6]);
-        load_page(posr[(du + 2) % 6], pgr[(du + 2) % 3]);
-        const int s = u % stages;
-        const uint32_t k = u / stages;
-        if (!warp_wait(bar(Ctl::kRawEmpty, s), (k & 1u) ^ 1u, abort_addr)) {
-          stop = true;
-          break;
-        }
-        int64_t off[2];
         bool val[2];
         int bad = 0;
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const int64_t pg = pgr[du % 3][j];
-          off[j] = pg >= 0 ? pg * p.block_stride +
-                                 static_cast<int64_t>(posr[du % 6][j] % p.page_size) * L::kRowBytes
-                           : -1;
-          val[j] = off[j] >= 0;
-          bad += pg == -2;
+          val[j] = pg[k][j] >= 0;
+          bad += pg[k][j] == -2;
+          const int64_t off = val[j] ? pg[k][j] * p.block_stride +
+                                           static_cast<int64_t>(posa[k][j] % p.page_size) *
+                                               L::kRowBytes
+                                     : 0;
+          st_shared_u32(offs_row(os) + 4 * (lane + 32 * j), static_cast<uint32_t>(off >> 4));
         }
         const uint32_t b0 = __ballot_sync(0xffffffffu, val[0]);
         const uint32_t b1 = __ballot_sync(0xffffffffu, val[1]);
@@ -528,35 +567,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bad = __reduce_add_sync(0xffffffffu, bad);
           if (lane == 0 && bad > 0 && p.invalid_count != nullptr) atomicAdd(p.invalid_count, bad);
         }
+        __syncwarp();
         if (lane == 0) {
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * s) = mask;
-          if (rank == 0)
-            *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 15)) =
-                mask;
+          *reinterpret_cast<volatile uint64_t*>(smem + (offs_mask(os) - sbase)) = mask;
+          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31)) =
+              mask;
+          mbar_arrive(bar(Ctl::kOffsFull, os));
         }
-        // Each lane copies its own two rows in 16-byte cp.async pieces on the
-        // load/store path (one bulk copy per 352-byte row serialises on the
-        // copy engine); the stage's barrier completes when every lane's copies
-        // have landed.
-        const uint32_t dst0 = raw_base + s * stage_bytes + raw_row_off(lane, copy);
-        const uint32_t dst1 = raw_base + s * stage_bytes + raw_row_off(lane + 32, copy);
-        const uint8_t* src0 = p.cache + (val[0] ? off[0] : 0);
-        const uint8_t* src1 = p.cache + (val[1] ? off[1] : 0);
-        for (int c = 0; c < copy; c += 16) {
-          if (val[0]) cp_async16(dst0 + c, src0 + c);
-          if (val[1]) cp_async16(dst1 + c, src1 + c);
-        }
-        cp_async_arrive_noinc(bar(Ctl::kRawFull, s));
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        posa[k][0] = posb[k][0];
+        posa[k][1] = posb[k][1];
       }
     }
+  } else if (warp >= kCopyWarp0 && warp < kDequantWarp0) {
+    // ------------------------------------------------ gather copies, ahead of the dequant
+    const int ct = tid - kCopyWarp0 * 32;
+    // score CTA: Q is staged over the raw ring until it has moved into TMEM
+    bool run = rank != 0 || warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
+    for (int u = 0; u < n_sub && run; ++u) run = issue_stage(u, ct);
   } else if (warp >= kDequantWarp0 && rank == 0) {
-    // ------------------------------------------------ score CTA dequant: K chunks
+    // ------------------------------------------------ score CTA: gather + K chunks
     // Chunk kb of tile i: rows 0..127 of the tile x dims [64 kb, 64 kb + 64)
     // (kb = 8: the 64 rope dims). Thread -> (row, half of the chunk's dims).
     const int dt = tid - kDequantWarp0 * 32;
     const int row = dt & 127;
     const int hf = dt >> 7;
-    bool run = warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
+    bool run = warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);  // Q staging overlaps the ring
     for (int i = 0; i < n_tiles && run; ++i) {
       const int ua = 2 * i, ub = 2 * i + 1;
       const int sa = ua % L::kStagesS, sb = ub % L::kStagesS;
@@ -564,48 +602,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           !warp_wait(bar(Ctl::kRawFull, sb), (ub / L::kStagesS) & 1u, abort_addr))
         break;
       const int sr = row < kSub ? sa : sb;
-      const uint64_t mask =
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * sr);
+      const int ur = row < kSub ? ua : ub;
+      const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(
+          smem + L::kCtl + Ctl::kMaskRing + 8 * (ur & 31));
       const bool ok = (mask >> (row & 63)) & 1ull;
       const uint32_t src = raw_base + sr * L::kStageS + raw_row_off(row & 63, L::kCopyS);
-#pragma unroll 1
-      for (int kb = 0; kb < kChunksPerTile; ++kb) {
+      // one chunk: wait for its ring slot, store 32 FP16 values, signal the MMA
+      auto put_chunk = [&](int kb, const uint32_t (&h)[16]) -> bool {
         const int q = i * kChunksPerTile + kb;
         const int cs = q % kChunkSlots;
-        if (!warp_wait(bar(Ctl::kChunkEmpty, cs), ((q / kChunkSlots) & 1u) ^ 1u, abort_addr)) {
-          run = false;
-          break;
-        }
-        uint32_t h[16];
-        if (!ok) {
-#pragma unroll
-          for (int x = 0; x < 16; ++x) h[x] = 0u;
-        } else if (L::kNv && kb < 8) {
-          const uint4 c = ld_shared_v4(src + 32 * kb + 16 * hf);
-          const uint32_t sc = ld_shared_u16(src + kScaleOff + 4 * kb + 2 * hf);
-          const uint32_t s0 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc & 0xFFu) * 0x0101u));
-          const uint32_t s1 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc >> 8) * 0x0101u));
-          const uint32_t w[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            uint32_t f[4];
-            e2m1x8_to_f16x8(w[x], f);
-            const uint32_t sx = x < 2 ? s0 : s1;
-#pragma unroll
-            for (int y = 0; y < 4; ++y) h[4 * x + y] = hmul2_u32(f[y], sx);
-          }
-        } else {
-          // E4M3 bytes: NVFP4 rope (row offset 288) or FP8 latent / rope (64 kb)
-          const uint32_t at = L::kNv ? kRopeOff + 32 * hf : 64 * kb + 32 * hf;
-          uint32_t lo[8], hi[8];
-          e4m3x16_to_f16(ld_shared_v4(src + at), lo);
-          e4m3x16_to_f16(ld_shared_v4(src + at + 16), hi);
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            h[x] = lo[x];
-            h[8 + x] = hi[x];
-          }
-        }
+        if (!warp_wait(bar(Ctl::kChunkEmpty, cs), ((q / kChunkSlots) & 1u) ^ 1u, abort_addr))
+          return false;
         const uint32_t dst = sbase + cs * L::kChunk;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -614,100 +621,134 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_cta();  // generic stores -> visible to the tensor core
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(Ctl::kChunkFull, cs));
+        return true;
+      };
+      if constexpr (L::kNv) {
+        // the whole half-row is loaded once per tile: 8 x 16 B codes, the 32
+        // scale bytes and 32 B of rope
+        uint4 pay[8], scv[2], rp[2];
+#pragma unroll
+        for (int kb = 0; kb < 8; ++kb)
+          pay[kb] = ok ? ld_shared_v4(src + 32 * kb + 16 * hf) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+          scv[x] = ok ? ld_shared_v4(src + kScaleOff + 16 * x) : make_uint4(0u, 0u, 0u, 0u);
+          rp[x] = ok ? ld_shared_v4(src + kRopeOff + 32 * hf + 16 * x) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        const uint32_t scw[8] = {scv[0].x, scv[0].y, scv[0].z, scv[0].w,
+                                 scv[1].x, scv[1].y, scv[1].z, scv[1].w};
+#pragma unroll
+        for (int kb = 0; kb < 8 && run; ++kb) {
+          const uint32_t sc = (scw[kb] >> (16 * hf)) & 0xFFFFu;
+          const uint32_t s0 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc & 0xFFu) * 0x0101u));
+          const uint32_t s1 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc >> 8) * 0x0101u));
+          const uint32_t w[4] = {pay[kb].x, pay[kb].y, pay[kb].z, pay[kb].w};
+          uint32_t h[16];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            uint32_t f[4];
+            e2m1x8_to_f16x8(w[x], f);
+            const uint32_t sx = x < 2 ? s0 : s1;
+#pragma unroll
+            for (int y = 0; y < 4; ++y) h[4 * x + y] = hmul2_u32(f[y], sx);
+          }
+          run = put_chunk(kb, h);
+        }
+        if (run) {
+          uint32_t h[16], lo[8], hi[8];
+          e4m3x16_to_f16(rp[0], lo);
+          e4m3x16_to_f16(rp[1], hi);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            h[x] = lo[x];
+            h[8 + x] = hi[x];
+          }
+          run = put_chunk(8, h);
+        }
+      } else {
+#pragma unroll 1
+        for (int kb = 0; kb < kChunksPerTile && run; ++kb) {
+          uint32_t h[16], lo[8], hi[8];
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          e4m3x16_to_f16(ok ? ld_shared_v4(src + 64 * kb + 32 * hf) : z, lo);
+          e4m3x16_to_f16(ok ? ld_shared_v4(src + 64 * kb + 32 * hf + 16) : z, hi);
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            h[x] = lo[x];
+            h[8 + x] = hi[x];
+          }
+          run = put_chunk(kb, h);
+        }
       }
+      if (!run) break;
       __syncwarp();
-      if (lane == 0 && run) {
+      if (lane == 0) {
         mbar_arrive(bar(Ctl::kRawEmpty, sa));
         mbar_arrive(bar(Ctl::kRawEmpty, sb));
       }
     }
   } else if (warp >= kDequantWarp0) {
-    // ------------------------------------------------ output CTA dequant: V^T tiles
-    // V^T [512 dims][64 rows]: one item = 8 rows x 16 dims; the transpose is
-    // done in registers (prmt pairs the same dim of two rows).
+    // ------------------------------------------------ output CTA: gather + V slots
+    // V (rows x 512 dims, FP16) is read by the P V MMA MN-major: each 32-row
+    // slot holds 8 blocks of 64 dims, each block 4 groups of 8 rows x 128 B.
+    // Thread item = (row, 16-dim group); 4 items per thread per slot.
     const int dt = tid - kDequantWarp0 * 32;
-    const int tg = dt & 7;  // row group (8 consecutive rows)
-    const int j = dt >> 3;  // 16-dim group 0..31
-    for (int u = 0; u < n_sub; ++u) {
+    bool run = true;
+    for (int u = 0; u < n_sub && run; ++u) {
       const int s = u % L::kStagesO;
-      const uint32_t k = u / L::kStagesO;
-      const int s2 = u & 1;
-      const uint32_t k2 = u >> 1;
-      if (!warp_wait(bar(Ctl::kRawFull, s), k & 1u, abort_addr)) break;
-      if (!warp_wait(bar(Ctl::kVtEmpty, s2), (k2 & 1u) ^ 1u, abort_addr)) break;
+      if (!warp_wait(bar(Ctl::kRawFull, s), (u / L::kStagesO) & 1u, abort_addr)) break;
       const uint64_t mask =
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kStageMask + 8 * s);
+          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31));
       const uint32_t raw = raw_base + s * L::kStageO;
-      const uint32_t vtile = sbase + s2 * L::kVTile;
-      if constexpr (L::kNv) {
-        uint32_t pw[8][2], scl[8];
-#pragma unroll
-        for (int tt = 0; tt < 8; ++tt) {
-          const int r = tg * 8 + tt;
-          const uint32_t rr = raw + raw_row_off(r, L::kCopyO);
-          const bool ok = (mask >> r) & 1ull;
-          const uint2 pl = ok ? ld_shared_v2(rr + j * 8) : make_uint2(0u, 0u);
-          pw[tt][0] = pl.x;
-          pw[tt][1] = pl.y;
-          const uint32_t sc = ok ? ld_shared_u8(rr + kScaleOff + j) : 0u;
-          scl[tt] = e4m3x2_to_f16x2(static_cast<uint16_t>(sc | (sc << 8)));
+#pragma unroll 1
+      for (int hh = 0; hh < 2; ++hh) {
+        const int hs = 2 * u + hh;
+        const int vs = hs % L::kVSlots;
+        if (!warp_wait(bar(Ctl::kVtEmpty, vs), ((hs / L::kVSlots) & 1u) ^ 1u, abort_addr)) {
+          run = false;
+          break;
         }
+        const uint32_t vslot = sbase + vs * L::kVSlot;
 #pragma unroll
-        for (int wi = 0; wi < 2; ++wi) {
-          uint32_t hh[8][4];
+        for (int it = 0; it < 4; ++it) {
+          const int item = dt + 256 * it;
+          const int r = item & 31;          // row within the slot
+          const int j = item >> 5;          // 16-dim group 0..31
+          const int rr = 32 * hh + r;       // row within the stage
+          const uint32_t rp = raw + raw_row_off(rr, L::kCopyO);
+          const bool ok = (mask >> rr) & 1ull;
+          uint32_t h[8];
+          if (!ok) {
 #pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            e2m1x8_to_f16x8(pw[tt][wi], hh[tt]);
+            for (int x = 0; x < 8; ++x) h[x] = 0u;
+          } else if constexpr (L::kNv) {
+            const uint2 pl = ld_shared_v2(rp + 8 * j);
+            const uint32_t sc = ld_shared_u8(rp + kScaleOff + j);
+            const uint32_t s2h = e4m3x2_to_f16x2(static_cast<uint16_t>(sc * 0x0101u));
+            uint32_t lo[4], hi[4];
+            e2m1x8_to_f16x8(pl.x, lo);
+            e2m1x8_to_f16x8(pl.y, hi);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) hh[tt][q] = hmul2_u32(hh[tt][q], scl[tt]);
+            for (int y = 0; y < 4; ++y) {
+              h[y] = hmul2_u32(lo[y], s2h);
+              h[4 + y] = hmul2_u32(hi[y], s2h);
+            }
+          } else {
+            e4m3x16_to_f16(ld_shared_v4(rp + 16 * j), h);
           }
-#pragma unroll
-          for (int bq = 0; bq < 4; ++bq) {
-            const uint32_t d0 = static_cast<uint32_t>(j * 16 + wi * 8 + 2 * bq);
-            st_shared_v4(vtile + sw128_off(d0, tg), prmt(hh[0][bq], hh[1][bq], 0x5410u),
-                         prmt(hh[2][bq], hh[3][bq], 0x5410u), prmt(hh[4][bq], hh[5][bq], 0x5410u),
-                         prmt(hh[6][bq], hh[7][bq], 0x5410u));
-            st_shared_v4(vtile + sw128_off(d0 + 1, tg), prmt(hh[0][bq], hh[1][bq], 0x7632u),
-                         prmt(hh[2][bq], hh[3][bq], 0x7632u), prmt(hh[4][bq], hh[5][bq], 0x7632u),
-                         prmt(hh[6][bq], hh[7][bq], 0x7632u));
-          }
+          // dims [16 j, 16 j + 16): block nb = j / 4, 16-byte chunks 2 (j % 4), +1
+          const uint32_t blk = vslot + (j >> 2) * 4096u;
+          const uint32_t c0 = static_cast<uint32_t>((j & 3) * 2);
+          st_shared_v4(blk + sw128_off(r, c0), h[0], h[1], h[2], h[3]);
+          st_shared_v4(blk + sw128_off(r, c0 + 1), h[4], h[5], h[6], h[7]);
         }
-      } else {
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t ww[8][2];
-#pragma unroll
-          for (int tt = 0; tt < 8; ++tt) {
-            const int r = tg * 8 + tt;
-            const uint32_t rr = raw + raw_row_off(r, L::kCopyO);
-            const bool ok = (mask >> r) & 1ull;
-            const uint2 v = ok ? ld_shared_v2(rr + j * 16 + half * 8) : make_uint2(0u, 0u);
-            ww[tt][0] = v.x;
-            ww[tt][1] = v.y;
-          }
-#pragma unroll
-          for (int pi = 0; pi < 4; ++pi) {  // byte pair pi -> dims 2pi, 2pi+1 of this half
-            uint32_t f[8];
-#pragma unroll
-            for (int tt = 0; tt < 8; ++tt)
-              f[tt] = e4m3x2_to_f16x2(
-                  static_cast<uint16_t>((ww[tt][pi >> 1] >> (16 * (pi & 1))) & 0xFFFFu));
-            const uint32_t d0 = static_cast<uint32_t>(j * 16 + half * 8 + 2 * pi);
-            st_shared_v4(vtile + sw128_off(d0, tg), prmt(f[0], f[1], 0x5410u),
-                         prmt(f[2], f[3], 0x5410u), prmt(f[4], f[5], 0x5410u),
-                         prmt(f[6], f[7], 0x5410u));
-            st_shared_v4(vtile + sw128_off(d0 + 1, tg), prmt(f[0], f[1], 0x7632u),
-                         prmt(f[2], f[3], 0x7632u), prmt(f[4], f[5], 0x7632u),
-                         prmt(f[6], f[7], 0x7632u));
-          }
-        }
+        fence_proxy_async_cta();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(Ctl::kVtFull, vs));
       }
-      fence_proxy_async_cta();
+      if (!run) break;
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(bar(Ctl::kVtFull, s2));
-        mbar_arrive(bar(Ctl::kRawEmpty, s));
-      }
+      if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, s));
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue (one thread)
@@ -753,7 +794,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int u = 0; u < n_sub; ++u) {
           const int s2 = u & 1;
           const uint32_t k2 = u >> 1;
-          if (!wait_bar(bar(Ctl::kVtFull, s2), k2 & 1u, abort_addr)) break;
+          const int ha = 2 * u, hb = 2 * u + 1;
+          const int va = ha % L::kVSlots, vb = hb % L::kVSlots;
+          if (!wait_bar(bar(Ctl::kVtFull, va), (ha / L::kVSlots) & 1u, abort_addr)) break;
+          if (!wait_bar(bar(Ctl::kVtFull, vb), (hb / L::kVSlots) & 1u, abort_addr)) break;
           if (!wait_bar(bar(Ctl::kPFull, s2), k2 & 1u, abort_addr)) break;
           const uint4 fl = ld_shared_v4(ctl + Ctl::kAF + s2 * kAFBytes + 512);
           if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
@@ -761,20 +805,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             ++n_corr;
           }
           tc_fence_after();
-          const uint32_t vtile = sbase + s2 * L::kVTile;
           const uint32_t ptile = sbase + L::kP + s2 * L::kPTile;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t adesc = sw128_desc(ptile + kk * 32u);
+            const uint32_t vslot = sbase + (kk < 2 ? va : vb) * L::kVSlot + (kk & 1) * 2048u;
 #pragma unroll
             for (int nh = 0; nh < 2; ++nh) {
-              const uint64_t bdesc = sw128_desc(vtile + nh * 32768u + kk * 32u);
+              const uint64_t bdesc = sw128_desc_mn(vslot + nh * 16384u);
               mma_ss(tmem + 256u * nh, adesc, bdesc, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          mma_commit(bar(Ctl::kVtEmpty, s2));
+          mma_commit(bar(Ctl::kVtEmpty, va));
+          mma_commit(bar(Ctl::kVtEmpty, vb));
           mma_commit(bar(Ctl::kPvDone, s2));
-          last_bar = bar(Ctl::kVtEmpty, s2);
+          last_bar = bar(Ctl::kPvDone, s2);
           last_parity = k2 & 1u;
           issued = true;
         }
@@ -845,9 +890,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       uint64_t masks[2];
       masks[0] = *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing +
-                                                        8 * ((2 * i) & 15));
+                                                        8 * ((2 * i) & 31));
       masks[1] = *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing +
-                                                        8 * ((2 * i + 1) & 15));
+                                                        8 * ((2 * i + 1) & 31));
 #pragma unroll 1
       for (int jj = 0; jj < 2; ++jj) {
         const int u = 2 * i + jj;
