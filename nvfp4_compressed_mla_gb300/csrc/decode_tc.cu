@@ -50,13 +50,11 @@ namespace nvfp4_mla {
 namespace {
 
 constexpr int kSub = 64;             // rows per gather stage / P sub-tile
-constexpr int kWarps = 16;
+constexpr int kWarps = 14;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kCopyWarp0 = 6;        // warps 6-7: gather copies
-constexpr int kCopyThreads = 64;
-constexpr int kDequantWarp0 = 8;     // warps 8-15: dequant
+constexpr int kDequantWarp0 = 6;     // warps 6-13: gather copies + dequant
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;      // score CTA: S buffers at columns 256 and 384
 constexpr int kChunkSlots = 4;
@@ -303,11 +301,6 @@ __device__ __forceinline__ void bulk_s2s(uint32_t dst_cluster, uint32_t src, uin
       "r"(src), "r"(bytes), "r"(bar_cluster)
       : "memory");
 }
-// The barrier's arrival by this thread fires once all of its earlier cp.async
-// copies have completed (the arrival is one of the barrier's expected count).
-__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
-}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -426,12 +419,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(bar(Ctl::kRawFull, s), kCopyThreads);  // one cp.async arrival per copy thread
+      mbar_init(bar(Ctl::kRawFull, s), 1);  // armed with the stage's bytes, then bulk copies
       mbar_init(bar(Ctl::kRawEmpty, s), 8);
     }
     for (int s = 0; s < L::kOffsSlots; ++s) {
       mbar_init(bar(Ctl::kOffsFull, s), 1);
-      mbar_init(bar(Ctl::kOffsEmpty, s), kCopyThreads / 32);
+      mbar_init(bar(Ctl::kOffsEmpty, s), 8);
     }
     for (int s = 0; s < kChunkSlots; ++s) {
       mbar_init(bar(Ctl::kChunkFull, s), 8);
@@ -473,29 +466,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto offs_row = [&](int slot) { return offs_base + slot * (kSub * 4); };
   auto offs_mask = [&](int slot) { return offs_base + L::kOffsSlots * (kSub * 4) + 8 * slot; };
 
-  // Copies of stage u (issued by the copy warps): consecutive threads
-  // take consecutive 16-byte pieces of the stage's rows, so a warp's copy
-  // instruction reads whole rows instead of 32 scattered pieces. The stage's
-  // barrier counts one arrival per thread, fired when its copies have landed.
+  // Copies of stage u, issued by the 8 dequant warps: lanes 0-7 of each warp
+  // issue one bulk copy (cp.async.bulk) per row. Random 352-byte rows are
+  // fetched fastest by many warps issuing a few row copies each (one warp
+  // issuing all of them serialises on the copy engine; 16-byte cp.async
+  // pieces cap the bytes in flight). The stage's barrier is armed with the
+  // stage's byte count by one thread and completes when every row landed.
   auto issue_stage = [&](int u, int dt) -> bool {
     const int os = u % L::kOffsSlots;
     const int s = u % stages;
     if (!warp_wait(bar(Ctl::kOffsFull, os), (u / L::kOffsSlots) & 1u, abort_addr)) return false;
     if (!warp_wait(bar(Ctl::kRawEmpty, s), ((u / stages) & 1u) ^ 1u, abort_addr)) return false;
     const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + (offs_mask(os) - sbase));
-    const int chunks = copy / 16;
-    const uint32_t dst = raw_base + s * stage_bytes;
-    for (int c = dt; c < kSub * chunks; c += kCopyThreads) {
-      const int r = c / chunks;
-      const int q = c - r * chunks;
+    const int ln = dt & 31, w = dt >> 5;
+    if (dt == 0) mbar_arrive_tx(bar(Ctl::kRawFull, s), __popcll(mask) * copy);
+    if (ln < 8) {
+      const int r = 8 * w + ln;
       if ((mask >> r) & 1ull) {
         const uint64_t src16 = ld_shared_u32(offs_row(os) + 4 * r);
-        cp_async16(dst + raw_row_off(r, copy) + 16 * q, p.cache + (src16 << 4) + 16 * q);
+        bulk_g2s(raw_base + s * stage_bytes + raw_row_off(r, copy), p.cache + (src16 << 4), copy,
+                 bar(Ctl::kRawFull, s));
       }
     }
-    cp_async_arrive_noinc(bar(Ctl::kRawFull, s));
     __syncwarp();
-    if ((tid & 31) == 0) mbar_arrive(bar(Ctl::kOffsEmpty, os));
+    if (ln == 0) mbar_arrive(bar(Ctl::kOffsEmpty, os));
     return true;
   };
 
@@ -581,12 +575,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         posa[k][1] = posb[k][1];
       }
     }
-  } else if (warp >= kCopyWarp0 && warp < kDequantWarp0) {
-    // ------------------------------------------------ gather copies, ahead of the dequant
-    const int ct = tid - kCopyWarp0 * 32;
-    // score CTA: Q is staged over the raw ring until it has moved into TMEM
-    bool run = rank != 0 || warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
-    for (int u = 0; u < n_sub && run; ++u) run = issue_stage(u, ct);
   } else if (warp >= kDequantWarp0 && rank == 0) {
     // ------------------------------------------------ score CTA: gather + K chunks
     // Chunk kb of tile i: rows 0..127 of the tile x dims [64 kb, 64 kb + 64)
@@ -595,6 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = dt & 127;
     const int hf = dt >> 7;
     bool run = warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);  // Q staging overlaps the ring
+    for (int u = 0; u < min(L::kStagesS, n_sub) && run; ++u) run = issue_stage(u, dt);
     for (int i = 0; i < n_tiles && run; ++i) {
       const int ua = 2 * i, ub = 2 * i + 1;
       const int sa = ua % L::kStagesS, sb = ub % L::kStagesS;
@@ -686,6 +675,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(Ctl::kRawEmpty, sa));
         mbar_arrive(bar(Ctl::kRawEmpty, sb));
       }
+      for (int u = ua + L::kStagesS; u <= ub + L::kStagesS && u < n_sub && run; ++u)
+        run = issue_stage(u, dt);
     }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------ output CTA: gather + V slots
@@ -694,6 +685,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Thread item = (row, 16-dim group); 4 items per thread per slot.
     const int dt = tid - kDequantWarp0 * 32;
     bool run = true;
+    for (int u = 0; u < min(L::kStagesO, n_sub) && run; ++u) run = issue_stage(u, dt);
     for (int u = 0; u < n_sub && run; ++u) {
       const int s = u % L::kStagesO;
       if (!warp_wait(bar(Ctl::kRawFull, s), (u / L::kStagesO) & 1u, abort_addr)) break;
@@ -749,6 +741,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!run) break;
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, s));
+      if (u + L::kStagesO < n_sub) run = issue_stage(u + L::kStagesO, dt);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue (one thread)
