@@ -32,12 +32,15 @@
 //
 // Both CTAs gather their own copy of the rows: a producer warp resolves
 // top-k slots through the block table (-1 and unresolvable slots issue no
-// load), keeping the index and block-table loads two sub-tiles ahead, and
-// copies each row in 16-byte cp.async pieces into a ring of 64-row stages. Eight dequant warps expand E2M1 x E4M3 (exact in FP16) into the
-// 128-byte-swizzled K-major layouts the MMAs read. One thread issues the
-// MMAs; commits signal mbarriers. Softmax: P = 2^(s - m_ref) with m_ref
-// raised only when a score exceeds it by more than 8 (so P <= 256 in FP16)
-// and O rescaled only on those (rare) sub-tiles.
+// load), batching the index and block-table loads four stages ahead, and
+// publishes per 64-slot stage the rows' byte offsets and a live-row mask.
+// Eight dequant warps issue one bulk copy per live row into a ring of
+// stages (the stage's mbarrier expects live rows x row bytes), then expand
+// E2M1 x E4M3 (exact in FP16) into the 128-byte-swizzled layouts the MMAs
+// read (K-major K chunks in the score CTA, MN-major V slots in the output
+// CTA). One thread issues the MMAs; commits signal mbarriers. Softmax:
+// P = 2^(s - m_ref) with m_ref raised only when a score exceeds it by more
+// than 8 (so P <= 256 in FP16) and O rescaled only on those (rare) tiles.
 //
 // Every wait is bounded (about a second of clock64 cycles); a wait that
 // runs out sets an abort flag, the roles unwind together, tensor memory is
