@@ -91,7 +91,9 @@ struct TcLayout {
   static constexpr int kOffsS = kRawS + kStagesS * kStageS;
   static constexpr int kEndS = kOffsS + kOffsBytes;
   static constexpr int kQStage = 0;               // start-up: Q (bf16) staged over the above
-  static constexpr int kQStageBytes = 128 * (kLatent + kRope) * 2;
+  static constexpr int kQPitch = kLatent * 2 + 16; // latent rows padded: conflict-free row reads
+  static constexpr int kQRopeStage = 128 * kQPitch;
+  static constexpr int kQStageBytes = kQRopeStage + 128 * kRope * 2;
   // output CTA
   static constexpr int kVSlot = 32 * 1024;        // 32 rows x 512 dims FP16 (MN-major)
   static constexpr int kVSlots = 3;
@@ -129,6 +131,10 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 __device__ __forceinline__ void mbar_arrive_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster_relaxed(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
@@ -289,8 +295,11 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Relaxed: the bytes that complete the phase arrive by the bulk copy's own
+// complete_tx, so no release ordering is needed (a release.cluster arrive
+// costs a cluster-wide fence of several hundred cycles).
 __device__ __forceinline__ void mbar_arrive_tx_cluster(uint32_t cluster_bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.release.cluster.shared::cluster.b64 _, [%0], %1;" ::
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;" ::
                    "r"(cluster_bar),
                "r"(bytes)
                : "memory");
@@ -348,11 +357,25 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
 }
 
 // Bounded wait; false when it ran out (or another thread of the CTA aborted).
+// try_wait with a suspend-time hint: a waiting thread sleeps until the phase
+// completes (or the hint expires) instead of spinning.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kSuspendNs)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t abort_addr) {
   if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_test(bar, parity)) return true;
+    if (mbar_wait_suspend(bar, parity)) return true;
     if (ld_shared_u32(abort_addr) != 0) return false;
     if (clock64() - t0 > kWaitCycles) {
       st_shared_u32(abort_addr, 1u);
@@ -441,7 +464,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(Ctl::kSFull, s), 1);
       mbar_init(bar(Ctl::kSEmpty, s), 128);
       mbar_init(bar(Ctl::kPFull, s), 1);
-      mbar_init(bar(Ctl::kPEmpty, s), 128);
+      mbar_init(bar(Ctl::kPEmpty, s), 4);
       mbar_init(bar(Ctl::kPvDone, s), 1);
     }
     mbar_init(bar(Ctl::kOCorr, 0), 128);
@@ -457,7 +480,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_after();
   cluster_sync();  // the peer's barriers exist before anyone arrives on them
   const uint32_t tmem = ld_shared_u32(ctl + Ctl::kTmem);
+  if (tmem != 0u && tid == 0) st_shared_u32(abort_addr, 1u);  // MMA operands assume base 0
 
+  if (rank == 0) {
+    // Q of this token, issued first and spread over all warps (a copy
+    // instruction stalls its warp for a while): latent row r by warp r % 14,
+    // lane r / 14, into a 1040-byte pitch; the rope rows by one copy.
+    const int H = p.num_heads;
+    const uint32_t qbar = bar(Ctl::kQFull, 0);
+    if (tid == 0) mbar_arrive_tx(qbar, static_cast<uint32_t>(H * (kLatent + kRope) * 2));
+    __syncwarp();
+    const uint16_t* qlat_t = p.q_lat + static_cast<int64_t>(t) * H * kLatent;
+    for (int r = lane * kWarps + warp; r < H && lane < 10; r += 32 * kWarps)
+      bulk_g2s(sbase + L::kQStage + r * L::kQPitch, qlat_t + static_cast<int64_t>(r) * kLatent,
+               kLatent * 2, qbar);
+    if (tid == 32)
+      bulk_g2s(sbase + L::kQStage + L::kQRopeStage, p.q_rope + static_cast<int64_t>(t) * H * kRope,
+               static_cast<uint32_t>(H * kRope * 2), qbar);
+  }
   const int32_t b = __ldg(p.q_seq + t);
   const int32_t len = (b >= 0 && b < p.num_seqs) ? __ldg(p.seq_lens + b) : 0;
   const int32_t* idx_row = p.topk_idx + static_cast<int64_t>(t) * p.topk;
@@ -753,13 +793,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool issued = false;
       if (rank == 0) {
         if (wait_bar(bar(Ctl::kQReady, 0), 0, abort_addr)) {
+          // Operands from loop-invariant bases: the allocation of all 512
+          // columns starts at TMEM address 0 (checked at set-up), the chunk
+          // ring at the start of shared memory; a descriptor's address field
+          // counts 16 bytes.
           const uint64_t qrope = sw128_desc(sbase + L::kQRope);
+          const uint64_t ring = sw128_desc(sbase);
           bool run = true;
           for (int i = 0; i < n_tiles && run; ++i) {
             const int s2 = i & 1;
             const uint32_t k2 = i >> 1;
             if (!wait_bar(bar(Ctl::kSEmpty, s2), (k2 & 1u) ^ 1u, abort_addr)) break;
-            const uint32_t dcol = tmem + kSCol + 128u * s2;
+            const uint32_t dcol = kSCol + 128u * s2;
             for (int kb = 0; kb < kChunksPerTile; ++kb) {
               const int q = i * kChunksPerTile + kb;
               const int cs = q % kChunkSlots;
@@ -768,14 +813,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 break;
               }
               tc_fence_after();
-              const uint32_t chunk = sbase + cs * L::kChunk;
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t bdesc = sw128_desc(chunk + 32u * kk);
-                if (kb < 8)
-                  mma_ts(dcol, tmem + 32u * kb + 8u * kk, bdesc, kIdescQK, (kb | kk) != 0);
-                else
-                  mma_ss(dcol, qrope + 2u * kk, bdesc, kIdescQK, 1u);
+              const uint64_t bd = ring + static_cast<uint64_t>(cs * (L::kChunk >> 4));
+              if (kb < 8) {
+                const uint32_t a = 32u * kb;
+                mma_ts(dcol, a, bd, kIdescQK, kb != 0);
+                mma_ts(dcol, a + 8u, bd + 2u, kIdescQK, 1u);
+                mma_ts(dcol, a + 16u, bd + 4u, kIdescQK, 1u);
+                mma_ts(dcol, a + 24u, bd + 6u, kIdescQK, 1u);
+              } else {
+                mma_ss(dcol, qrope, bd, kIdescQK, 1u);
+                mma_ss(dcol, qrope + 2u, bd + 2u, kIdescQK, 1u);
+                mma_ss(dcol, qrope + 4u, bd + 4u, kIdescQK, 1u);
+                mma_ss(dcol, qrope + 6u, bd + 6u, kIdescQK, 1u);
               }
               mma_commit(bar(Ctl::kChunkEmpty, cs));
               last_bar = bar(Ctl::kChunkEmpty, cs);
@@ -828,26 +877,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     bool ok;
     {
-      // Q (bf16) of this token arrives by two bulk copies over the still
-      // unused buffers; each thread converts its head's row to FP16 (scales
-      // folded in): the latent part into TMEM, the rope part into the
+      // Q (bf16) of this token arrives by the copies issued at set-up over the
+      // still unused buffers; each thread converts its head's row to FP16
+      // (scales folded in): the latent part into TMEM, the rope part into the
       // swizzled shared-memory operand.
       const uint32_t qbar = bar(Ctl::kQFull, 0);
-      const uint32_t lat_bytes = static_cast<uint32_t>(p.num_heads) * (kLatent * 2);
-      const uint32_t rope_at = sbase + L::kQStage + 128u * kLatent * 2;
-      if (tid == 0) {
-        mbar_arrive_tx(qbar, lat_bytes + static_cast<uint32_t>(p.num_heads) * (kRope * 2));
-        bulk_g2s(sbase + L::kQStage, p.q_lat + static_cast<int64_t>(t) * p.num_heads * kLatent,
-                 lat_bytes, qbar);
-        bulk_g2s(rope_at, p.q_rope + static_cast<int64_t>(t) * p.num_heads * kRope,
-                 static_cast<uint32_t>(p.num_heads) * (kRope * 2), qbar);
-      }
-      ok = group_and(wait_bar(qbar, 0, abort_addr));
+      const uint32_t rope_at = sbase + L::kQStage + L::kQRopeStage;
+      ok = group_and(wait_bar(qbar, 0, abort_addr));  // copies issued at set-up
       const bool live = ok && h < p.num_heads;
 #pragma unroll 1
       for (int c = 0; c < 8; ++c) {
         uint32_t r[32];
-        const uint32_t src = sbase + L::kQStage + h * (kLatent * 2) + c * 128;
+        const uint32_t src = sbase + L::kQStage + h * L::kQPitch + c * 128;
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x = bf16x8_to_f16x8(
@@ -990,9 +1031,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      // this thread has read buffer s2's flags and factor (for sub-tile u, in the
-      // previous iteration): the score CTA may refill it
-      mbar_arrive_cluster(peer_ctl + Ctl::kPEmpty + 8 * s2);
+      // this warp has read buffer s2's flags and factors (for sub-tile u, in
+      // the previous iteration): the score CTA may refill it. The reads have
+      // completed (their values decided this warp's work), so a relaxed
+      // arrive suffices.
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster_relaxed(peer_ctl + Ctl::kPEmpty + 8 * s2);
       if (u + 1 < n_sub) {
         const int n2 = (u + 1) & 1;
         const uint32_t nk2 = (u + 1) >> 1;
@@ -1036,37 +1080,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool single = p.num_splits == 1;
       const float sc = single ? inv * p.out_mult : inv;
       const int64_t part = (static_cast<int64_t>(t) * p.num_splits + split) * p.num_heads + h;
+      // Rows leave through shared memory (V slots and P tiles are idle now):
+      // each thread stages its head's row at a padded pitch (conflict-free),
+      // then each warp writes its 32 rows with stores that are contiguous
+      // across the warp. fp32 rows (fp32 output, split-K partials) go in two
+      // halves of 256 columns so the staging stays within 133 KB.
+      const bool f32 = !(single && !p.out_fp32);
+      constexpr uint32_t kOutPitch = 1024 + 16;
+      const uint32_t stg = sbase + static_cast<uint32_t>(h) * kOutPitch;
+      const int H = p.num_heads;
 #pragma unroll 1
-      for (int cc = 0; cc < 16; ++cc) {
-        uint32_t r[32];
-        if (ok) {
-          tmem_ld32(tmem + lane_base + 32u * cc, r);
-          tmem_ld_wait();
-        } else {
+      for (int hv = 0; hv < (f32 ? 2 : 1); ++hv) {
+#pragma unroll 1
+        for (int cc = 0; cc < (f32 ? 8 : 16); ++cc) {
+          uint32_t r[32];
+          if (ok) {
+            tmem_ld32(tmem + lane_base + 256u * hv + 32u * cc, r);
+            tmem_ld_wait();
+          } else {
 #pragma unroll
-          for (int q = 0; q < 32; ++q) r[q] = 0u;
+            for (int q = 0; q < 32; ++q) r[q] = 0u;
+          }
+          float v[32];
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(r[q]) * sc;
+          if (!f32) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              st_shared_v4(stg + cc * 64 + q * 16, pack_bf16x2(v[8 * q], v[8 * q + 1]),
+                           pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                           pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                           pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              st_shared_v4(stg + cc * 128 + q * 16, __float_as_uint(v[4 * q]),
+                           __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
+                           __float_as_uint(v[4 * q + 3]));
+          }
         }
-        if (!live) continue;
-        float v[32];
+        __syncwarp();
+        // the warp's rows, 1 KB each (a bf16 row or an fp32 half row)
+#pragma unroll 1
+        for (int rr = 0; rr < 32; ++rr) {
+          const int hh = warp * 32 + rr;
+          if (hh >= H) break;
+          const int64_t qhh = static_cast<int64_t>(t) * H + hh;
+          const int64_t phh = (static_cast<int64_t>(t) * p.num_splits + split) * H + hh;
+          uint8_t* dst = !f32 ? reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) + qhh * kLatent)
+                         : single ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) + qhh * kLatent + 256 * hv)
+                                  : reinterpret_cast<uint8_t*>(p.ws + phh * kLatent + 256 * hv);
+          const uint32_t src = sbase + static_cast<uint32_t>(hh) * kOutPitch;
 #pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(r[q]) * sc;
-        if (single && !p.out_fp32) {
-          uint4* dst =
-              reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + qh * kLatent + cc * 32);
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]),
-                                pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                                pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-        } else {
-          float* dst = single ? static_cast<float*>(p.out) + qh * kLatent + cc * 32
-                              : p.ws + part * kLatent + cc * 32;
-#pragma unroll
-          for (int q = 0; q < 8; ++q)
-            reinterpret_cast<float4*>(dst)[q] =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int k = 0; k < 2; ++k)
+            *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) = ld_shared_v4(src + k * 512 + lane * 16);
         }
+        __syncwarp();  // the next half overwrites this warp's staging rows
       }
       if (live) {
         if (single) {
