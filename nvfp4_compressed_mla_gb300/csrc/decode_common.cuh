@@ -31,6 +31,7 @@ struct DecodeParams {
   float* ws;          // [num_q, splits, H, 512] partial O, then [num_q, splits, H] partial LSE
   int32_t num_splits, tiles_per_split, num_tiles;
   int32_t* invalid_count;
+  int32_t use_tma;    // rows gathered with tile::gather4 tensor copies (else one bulk copy per row)
 };
 
 // Enqueue the tensor-core decode kernel (one 2-CTA cluster per (token, split)).

@@ -45,7 +45,11 @@
 // Every wait is bounded (about a second of clock64 cycles); a wait that
 // runs out sets an abort flag, the roles unwind together, tensor memory is
 // freed, and the unit's outputs are written as NaN.
+#include <cuda.h>
 #include <math.h>
+#include <string.h>
+
+#include <mutex>
 
 #include "decode_common.cuh"
 
@@ -53,11 +57,12 @@ namespace nvfp4_mla {
 namespace {
 
 constexpr int kSub = 64;             // rows per gather stage / P sub-tile
-constexpr int kWarps = 14;
+constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 6;     // warps 6-13: gather copies + dequant
+constexpr int kDequantWarp0 = 6;     // warps 6-13: dequant
+constexpr int kIssueWarp0 = 14;      // warps 14-15: gather copies
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;      // score CTA: S buffers at columns 256 and 384
 constexpr int kChunkSlots = 4;
@@ -73,15 +78,25 @@ template <int kFmt>
 struct TcLayout {
   static constexpr bool kNv = kFmt == NVFP4_MLA_ROW_NVFP4_352;
   static constexpr int kRowBytes = kNv ? kNvfp4Row : kFp8Row;
-  static constexpr int kCopyS = kRowBytes;        // score CTA copies whole rows
-  static constexpr int kCopyO = kNv ? 288 : 512;  // output CTA: latent part (+ scales)
-  static constexpr int kPad = 16;                 // per 8-row group, against bank conflicts
-  static constexpr int kStageS = kSub * kCopyS + 8 * kPad;
-  static constexpr int kStageO = kSub * kCopyO + 8 * kPad;
-  static constexpr int kStagesS = kNv ? 4 : 3;
+  // Gathered rows: the score CTA keeps whole rows, the output CTA the latent
+  // part (plus 16 bytes); both padded to an odd number of 16-byte units so
+  // eight consecutive rows hit distinct bank groups. Tensor copies write
+  // groups of four rows; groups start 128-byte aligned.
+  static constexpr int kElem = kNv ? 2 : 4;                 // tensor-map element bytes
+  static constexpr int kRowElems = kRowBytes / kElem;       // 176 / 144
+  static constexpr int kRowS = kNv ? 368 : 592;             // whole row + 16 zero-filled bytes
+  static constexpr int kRowO = kNv ? 304 : 528;             // latent (+ 16 bytes of the rope)
+  static constexpr int kCopyS = kRowBytes;                  // per-row copies (fallback)
+  static constexpr int kCopyO = kNv ? 288 : 512;
+  static constexpr int kGroupS = (4 * kRowS + 127) / 128 * 128;  // 1536 / 2432
+  static constexpr int kGroupO = (4 * kRowO + 127) / 128 * 128;  // 1280 / 2176
+  static constexpr int kStageS = 16 * kGroupS;
+  static constexpr int kStageO = 16 * kGroupO;
+  static constexpr int kStagesS = kNv ? 4 : 2;
   static constexpr int kStagesO = kNv ? 3 : 2;
-  static constexpr int kOffsSlots = kNv ? 8 : 6;  // resolved row offsets, 64 per slot
-  static constexpr int kOffsBytes = kOffsSlots * (kSub * 4 + 8);
+  static constexpr int kOffsSlots = kNv ? 8 : 6;  // resolved stages: 64 byte offsets + live mask
+  static constexpr int kOffsSlot = kSub * 8 + 8;
+  static constexpr int kOffsBytes = kOffsSlots * kOffsSlot;
   // score CTA
   static constexpr int kChunk = 16384;            // 128 rows x 64 dims FP16
   static constexpr int kQRope = kChunkSlots * kChunk;
@@ -107,7 +122,9 @@ struct TcLayout {
   static constexpr int kBytes = kCtl + kCtlBytes;
   static_assert(kBytes <= 232448, "shared memory budget");
   static_assert(kQStageBytes <= kRawS + kStagesS * kStageS, "Q staging fits the score CTA's buffers");
-  static_assert(kStageS % 16 == 0 && kStageO % 16 == 0 && kP % 1024 == 0, "alignment");
+  static_assert(kStageS % 128 == 0 && kStageO % 128 == 0 && kP % 1024 == 0, "alignment");
+  static_assert(kRawS % 128 == 0 && kRawO % 128 == 0, "tensor-copy destinations");
+  static_assert(128 * (1024 + 16) <= kRawO + kStagesO * kStageO, "epilogue staging fits");
 };
 
 // control block: same offset in both CTAs of the cluster
@@ -333,6 +350,24 @@ __device__ __forceinline__ bool group_and(bool v) {
 }
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+// four rows (y0..y3) of a 2-D tensor map, one box each, into consecutive boxes at dst
+__device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* tm, int32_t y0, int32_t y1,
+                                        int32_t y2, int32_t y3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tm)), "r"(0), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr) {
+  uint64_t v;
+  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
+  asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
 // 1024 bytes apart (stride byte offset), descriptor version 1.
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
@@ -398,9 +433,6 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ uint32_t raw_row_off(int r, int copy) {
-  return static_cast<uint32_t>(r * copy + (r >> 3) * 16);
-}
 
 // FP16x2 of two fp32 p values and the conversions of the Q rows.
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, float m) {
@@ -423,7 +455,8 @@ __device__ __forceinline__ void e4m3x16_to_f16(uint4 v, uint32_t (&h)[8]) {
 // ------------------------------------------------------------------ kernel
 template <int kFmt>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_tc_kernel(const DecodeParams p) {
+    decode_tc_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tm_s,
+                     const __grid_constant__ CUtensorMap tm_o) {
   using L = TcLayout<kFmt>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
@@ -450,7 +483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < L::kOffsSlots; ++s) {
       mbar_init(bar(Ctl::kOffsFull, s), 1);
-      mbar_init(bar(Ctl::kOffsEmpty, s), 8);
+      mbar_init(bar(Ctl::kOffsEmpty, s), 2);  // one arrival per copy-issuing warp
     }
     for (int s = 0; s < kChunkSlots; ++s) {
       mbar_init(bar(Ctl::kChunkFull, s), 8);
@@ -501,42 +534,71 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int32_t b = __ldg(p.q_seq + t);
   const int32_t len = (b >= 0 && b < p.num_seqs) ? __ldg(p.seq_lens + b) : 0;
   const int32_t* idx_row = p.topk_idx + static_cast<int64_t>(t) * p.topk;
-  const int copy = rank == 0 ? L::kCopyS : L::kCopyO;
+  const uint32_t copy = rank == 0 ? L::kCopyS : L::kCopyO;
   const uint32_t raw_base = sbase + (rank == 0 ? L::kRawS : L::kRawO);
   const uint32_t stage_bytes = rank == 0 ? L::kStageS : L::kStageO;
+  const uint32_t group_bytes = rank == 0 ? L::kGroupS : L::kGroupO;
+  const uint32_t row_pad = rank == 0 ? L::kRowS : L::kRowO;
+  auto raw_row = [&](int s, int r) {  // row r of gather stage s
+    return raw_base + s * stage_bytes + (r >> 2) * group_bytes + (r & 3) * row_pad;
+  };
 
   const uint32_t offs_base = sbase + (rank == 0 ? L::kOffsS : L::kOffsO);
-  auto offs_row = [&](int slot) { return offs_base + slot * (kSub * 4); };
-  auto offs_mask = [&](int slot) { return offs_base + L::kOffsSlots * (kSub * 4) + 8 * slot; };
+  auto offs_row = [&](int slot) { return offs_base + slot * L::kOffsSlot; };
+  auto offs_mask = [&](int slot) { return offs_base + slot * L::kOffsSlot + kSub * 8; };
 
-  // Copies of stage u, issued by the 8 dequant warps: lanes 0-7 of each warp
-  // issue one bulk copy (cp.async.bulk) per row. Random 352-byte rows are
-  // fetched fastest by many warps issuing a few row copies each (one warp
-  // issuing all of them serialises on the copy engine; 16-byte cp.async
-  // pieces cap the bytes in flight). The stage's barrier is armed with the
-  // stage's byte count by one thread and completes when every row landed.
-  auto issue_stage = [&](int u, int dt) -> bool {
+  // Copies of stage u, issued by the two copy warps (iw = 0, 1) as soon as
+  // the stage is resolved and its ring slot released. Tensor path: lanes 0-7
+  // of warp iw issue the gather4 copies of row groups 8 iw .. 8 iw + 7 (a
+  // group with no live row is skipped; dead rows of a live group re-read one
+  // of its live rows). Fallback (a page stride that is not a whole number of
+  // rows): lane l of warp iw copies row 32 iw + l when live. A copy
+  // instruction stalls its warp for a while, hence dedicated warps. One thread
+  // arms the stage's barrier with the stage's byte count.
+  const CUtensorMap* tmap = rank == 0 ? &tm_s : &tm_o;
+  auto issue_stage = [&](int u, int iw) -> bool {
     const int os = u % L::kOffsSlots;
     const int s = u % stages;
     if (!warp_wait(bar(Ctl::kOffsFull, os), (u / L::kOffsSlots) & 1u, abort_addr)) return false;
     if (!warp_wait(bar(Ctl::kRawEmpty, s), ((u / stages) & 1u) ^ 1u, abort_addr)) return false;
-    const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(smem + (offs_mask(os) - sbase));
-    const int ln = dt & 31, w = dt >> 5;
-    if (dt == 0) mbar_arrive_tx(bar(Ctl::kRawFull, s), __popcll(mask) * copy);
-    if (ln < 8) {
-      const int r = 8 * w + ln;
-      if ((mask >> r) & 1ull) {
-        const uint64_t src16 = ld_shared_u32(offs_row(os) + 4 * r);
-        bulk_g2s(raw_base + s * stage_bytes + raw_row_off(r, copy), p.cache + (src16 << 4), copy,
-                 bar(Ctl::kRawFull, s));
+    const uint64_t mask = ld_shared_u64(offs_mask(os));
+    const uint32_t full = bar(Ctl::kRawFull, s);
+    if (p.use_tma) {
+      const uint64_t any = (mask | (mask >> 1) | (mask >> 2) | (mask >> 3)) & 0x1111111111111111ull;
+      if (iw == 0 && lane == 0)
+        mbar_arrive_tx(full, static_cast<uint32_t>(__popcll(any)) * 4u * row_pad);
+      if (lane < 8) {
+        const int g = 8 * iw + lane;
+        const uint32_t m4 = static_cast<uint32_t>(mask >> (4 * g)) & 15u;
+        if (m4 != 0u) {
+          const int first = 4 * g + __ffs(m4) - 1;
+          int32_t y[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int r = ((m4 >> k) & 1u) ? 4 * g + k : first;
+            y[k] = static_cast<int32_t>(ld_shared_u64(offs_row(os) + 8 * r) / L::kRowBytes);
+          }
+          gather4(raw_row(s, 4 * g), tmap, y[0], y[1], y[2], y[3], full);
+        }
       }
+    } else {
+      if (iw == 0 && lane == 0)
+        mbar_arrive_tx(full, static_cast<uint32_t>(__popcll(mask)) * copy);
+      const int r = 32 * iw + lane;
+      if ((mask >> r) & 1ull)
+        bulk_g2s(raw_row(s, r), p.cache + ld_shared_u64(offs_row(os) + 8 * r), copy, full);
     }
     __syncwarp();
-    if (ln == 0) mbar_arrive(bar(Ctl::kOffsEmpty, os));
+    if (lane == 0) mbar_arrive(bar(Ctl::kOffsEmpty, os));
     return true;
   };
 
-  if (warp == kProducerWarp) {
+  if (warp >= kIssueWarp0) {
+    // ------------------------------------------------ gather copies
+    // (score CTA: Q is staged over the ring until it is converted)
+    bool run = rank != 0 || warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
+    for (int u = 0; u < n_sub && run; ++u) run = issue_stage(u, warp - kIssueWarp0);
+  } else if (warp == kProducerWarp) {
     // ------------------------------------------------ resolve: slots -> row offsets
     // Index and block-table loads are dependent global loads; four stages are
     // resolved per batch with all their loads in flight together, and the
@@ -595,7 +657,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                            static_cast<int64_t>(posa[k][j] % p.page_size) *
                                                L::kRowBytes
                                      : 0;
-          st_shared_u32(offs_row(os) + 4 * (lane + 32 * j), static_cast<uint32_t>(off >> 4));
+          st_shared_u64(offs_row(os) + 8 * (lane + 32 * j), static_cast<uint64_t>(off));
         }
         const uint32_t b0 = __ballot_sync(0xffffffffu, val[0]);
         const uint32_t b1 = __ballot_sync(0xffffffffu, val[1]);
@@ -606,7 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         if (lane == 0) {
-          *reinterpret_cast<volatile uint64_t*>(smem + (offs_mask(os) - sbase)) = mask;
+          st_shared_u64(offs_mask(os), mask);
           *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31)) =
               mask;
           mbar_arrive(bar(Ctl::kOffsFull, os));
@@ -626,7 +688,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int row = dt & 127;
     const int hf = dt >> 7;
     bool run = warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);  // Q staging overlaps the ring
-    for (int u = 0; u < min(L::kStagesS, n_sub) && run; ++u) run = issue_stage(u, dt);
     for (int i = 0; i < n_tiles && run; ++i) {
       const int ua = 2 * i, ub = 2 * i + 1;
       const int sa = ua % L::kStagesS, sb = ub % L::kStagesS;
@@ -638,7 +699,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(
           smem + L::kCtl + Ctl::kMaskRing + 8 * (ur & 31));
       const bool ok = (mask >> (row & 63)) & 1ull;
-      const uint32_t src = raw_base + sr * L::kStageS + raw_row_off(row & 63, L::kCopyS);
+      const uint32_t src = raw_row(sr, row & 63);
       // one chunk: wait for its ring slot, store 32 FP16 values, signal the MMA
       auto put_chunk = [&](int kb, const uint32_t (&h)[16]) -> bool {
         const int q = i * kChunksPerTile + kb;
@@ -714,12 +775,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!run) break;
       __syncwarp();
-      if (lane == 0) {
+      if (lane == 0) {  // stages sa and sb have been read: the copy warps may refill them
         mbar_arrive(bar(Ctl::kRawEmpty, sa));
         mbar_arrive(bar(Ctl::kRawEmpty, sb));
       }
-      for (int u = ua + L::kStagesS; u <= ub + L::kStagesS && u < n_sub && run; ++u)
-        run = issue_stage(u, dt);
     }
   } else if (warp >= kDequantWarp0) {
     // ------------------------------------------------ output CTA: gather + V slots
@@ -728,13 +787,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // Thread item = (row, 16-dim group); 4 items per thread per slot.
     const int dt = tid - kDequantWarp0 * 32;
     bool run = true;
-    for (int u = 0; u < min(L::kStagesO, n_sub) && run; ++u) run = issue_stage(u, dt);
     for (int u = 0; u < n_sub && run; ++u) {
       const int s = u % L::kStagesO;
       if (!warp_wait(bar(Ctl::kRawFull, s), (u / L::kStagesO) & 1u, abort_addr)) break;
       const uint64_t mask =
           *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31));
-      const uint32_t raw = raw_base + s * L::kStageO;
 #pragma unroll 1
       for (int hh = 0; hh < 2; ++hh) {
         const int hs = 2 * u + hh;
@@ -750,7 +807,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int r = item & 31;          // row within the slot
           const int j = item >> 5;          // 16-dim group 0..31
           const int rr = 32 * hh + r;       // row within the stage
-          const uint32_t rp = raw + raw_row_off(rr, L::kCopyO);
+          const uint32_t rp = raw_row(s, rr);
           const bool ok = (mask >> rr) & 1ull;
           uint32_t h[8];
           if (!ok) {
@@ -783,8 +840,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (!run) break;
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, s));
-      if (u + L::kStagesO < n_sub) run = issue_stage(u + L::kStagesO, dt);
+      if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, s));  // stage s read: the copy warps refill it
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue (one thread)
@@ -1158,13 +1214,88 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync();  // no peer access to this CTA's shared memory after this point
 }
 
+// cuTensorMapEncodeTiled, looked up once through the runtime
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+// The pool seen as a 2-D tensor of rows (row stride = row bytes), valid when
+// the page stride is a whole number of rows; one map per gathered row width.
+// The last pool seen by a host thread is cached with its maps.
+struct RowMaps {
+  const void* cache = nullptr;
+  int64_t rows = 0;
+  int fmt = -1;
+  bool ok = false;
+  CUtensorMap s, o;
+};
+thread_local RowMaps t_row_maps;
+
+template <int kFmt>
+bool row_maps(const DecodeParams& p, CUtensorMap* ms, CUtensorMap* mo) {
+  using L = TcLayout<kFmt>;
+  if (p.block_stride % L::kRowBytes != 0) return false;
+  const int64_t rows = p.num_blocks * (p.block_stride / L::kRowBytes);
+  if (rows <= 0 || rows > 0x7FFFFFFFll) return false;
+  RowMaps& c = t_row_maps;
+  if (!(c.cache == p.cache && c.rows == rows && c.fmt == kFmt)) {
+    c.cache = p.cache;
+    c.rows = rows;
+    c.fmt = kFmt;
+    c.ok = false;
+    EncodeTiledFn enc = encode_tiled();
+    if (enc != nullptr) {
+      const CUtensorMapDataType dt = L::kElem == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_UINT32;
+      const cuuint64_t dims[2] = {static_cast<cuuint64_t>(L::kRowElems),
+                                  static_cast<cuuint64_t>(rows)};
+      const cuuint64_t strides[1] = {static_cast<cuuint64_t>(L::kRowBytes)};
+      const cuuint32_t es[2] = {1, 1};
+      // score rows: whole row + 16 bytes past its end (out of range: zero-filled)
+      const cuuint32_t box_s[2] = {static_cast<cuuint32_t>(L::kRowS / L::kElem), 1};
+      // output rows: the latent part + 16 bytes of the rope (in range)
+      const cuuint32_t box_o[2] = {static_cast<cuuint32_t>(L::kRowO / L::kElem), 1};
+      void* base = const_cast<uint8_t*>(p.cache);
+      c.ok = enc(&c.s, dt, 2, base, dims, strides, box_s, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+             enc(&c.o, dt, 2, base, dims, strides, box_o, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    }
+  }
+  if (!c.ok) return false;
+  *ms = c.s;
+  *mo = c.o;
+  return true;
+}
+
 template <int kFmt>
 int32_t launch_fmt(const DecodeParams& p, cudaStream_t stream) {
   constexpr int smem = TcLayout<kFmt>::kBytes;
   cudaFuncSetAttribute(decode_tc_kernel<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   const int64_t ctas = 2ll * p.num_q * p.num_splits;
   if (ctas > 0x7FFFFFFF) return NVFP4_MLA_ERR_SHAPE;
-  decode_tc_kernel<kFmt><<<static_cast<unsigned>(ctas), kThreads, smem, stream>>>(p);
+  DecodeParams q = p;
+  CUtensorMap ms, mo;
+  memset(&ms, 0, sizeof(ms));
+  memset(&mo, 0, sizeof(mo));
+  q.use_tma = row_maps<kFmt>(p, &ms, &mo) ? 1 : 0;
+  decode_tc_kernel<kFmt><<<static_cast<unsigned>(ctas), kThreads, smem, stream>>>(q, ms, mo);
   return launch_status();
 }
 
