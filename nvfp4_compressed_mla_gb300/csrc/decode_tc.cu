@@ -434,6 +434,32 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity) {
 }
 
 
+// Packed fp32 pairs (sm_100 family): one instruction does two lanes' worth
+// of fma / add; three-input max.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f32x2_split(uint64_t v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // FP16x2 of two fp32 p values and the conversions of the Q rows.
 __device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 x, float m) {
   return make_uint4(pack_f16x2(bf16_lo(x.x) * m, bf16_hi(x.x) * m),
@@ -717,25 +743,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       if constexpr (L::kNv) {
-        // the whole half-row is loaded once per tile: 8 x 16 B codes, the 32
-        // scale bytes and 32 B of rope
-        uint4 pay[8], scv[2], rp[2];
+        // One rolled loop over the 8 latent chunks (a single copy of the
+        // body keeps the hot code small); chunk kb + 1's 16 bytes of codes
+        // and 4 scale bytes are loaded while chunk kb is converted.
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+        uint4 rp[2];
 #pragma unroll
-        for (int kb = 0; kb < 8; ++kb)
-          pay[kb] = ok ? ld_shared_v4(src + 32 * kb + 16 * hf) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-          scv[x] = ok ? ld_shared_v4(src + kScaleOff + 16 * x) : make_uint4(0u, 0u, 0u, 0u);
-          rp[x] = ok ? ld_shared_v4(src + kRopeOff + 32 * hf + 16 * x) : make_uint4(0u, 0u, 0u, 0u);
-        }
-        const uint32_t scw[8] = {scv[0].x, scv[0].y, scv[0].z, scv[0].w,
-                                 scv[1].x, scv[1].y, scv[1].z, scv[1].w};
-#pragma unroll
+        for (int x = 0; x < 2; ++x) rp[x] = ok ? ld_shared_v4(src + kRopeOff + 32 * hf + 16 * x) : z;
+        uint4 pay = ok ? ld_shared_v4(src + 16 * hf) : z;
+        uint32_t scw = ok ? ld_shared_u32(src + kScaleOff) : 0u;
+#pragma unroll 1
         for (int kb = 0; kb < 8 && run; ++kb) {
-          const uint32_t sc = (scw[kb] >> (16 * hf)) & 0xFFFFu;
+          const int kn = kb < 7 ? kb + 1 : kb;
+          const uint4 pay_n = ok ? ld_shared_v4(src + 32 * kn + 16 * hf) : z;
+          const uint32_t scw_n = ok ? ld_shared_u32(src + kScaleOff + 4 * kn) : 0u;
+          const uint32_t sc = (scw >> (16 * hf)) & 0xFFFFu;
           const uint32_t s0 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc & 0xFFu) * 0x0101u));
           const uint32_t s1 = e4m3x2_to_f16x2(static_cast<uint16_t>((sc >> 8) * 0x0101u));
-          const uint32_t w[4] = {pay[kb].x, pay[kb].y, pay[kb].z, pay[kb].w};
+          const uint32_t w[4] = {pay.x, pay.y, pay.z, pay.w};
           uint32_t h[16];
 #pragma unroll
           for (int x = 0; x < 4; ++x) {
@@ -746,6 +771,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int y = 0; y < 4; ++y) h[4 * x + y] = hmul2_u32(f[y], sx);
           }
           run = put_chunk(kb, h);
+          pay = pay_n;
+          scw = scw_n;
         }
         if (run) {
           uint32_t h[16], lo[8], hi[8];
@@ -978,7 +1005,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_tiles && ok; ++i) {
       const int s2 = i & 1;
       const uint32_t k2 = i >> 1;
-      ok = group_and(wait_bar(bar(Ctl::kSFull, s2), k2 & 1u, abort_addr));
+      ok = group_and(ok && wait_bar(bar(Ctl::kSFull, s2), k2 & 1u, abort_addr));
       if (!ok) break;
       tc_fence_after();
       uint64_t masks[2];
@@ -1001,9 +1028,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // raw max over the valid rows (the scale c > 0 is applied once after)
         float mx = -INFINITY;
         if (mask == ~0ull) {
+          float ma = -INFINITY, mb = -INFINITY;
 #pragma unroll
-          for (int q = 0; q < 32; ++q)
-            mx = fmaxf(mx, fmaxf(__uint_as_float(sa[q]), __uint_as_float(sb[q])));
+          for (int q = 0; q < 32; q += 2) {
+            ma = fmax3(ma, __uint_as_float(sa[q]), __uint_as_float(sb[q]));
+            mb = fmax3(mb, __uint_as_float(sa[q + 1]), __uint_as_float(sb[q + 1]));
+          }
+          mx = fmaxf(ma, mb);
         } else {
 #pragma unroll
           for (int q = 0; q < 32; ++q) {
@@ -1025,49 +1056,61 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         const float neg_m = m_ref == -INFINITY ? 0.f : -m_ref;
         const bool none = m_ref == -INFINITY;
-        uint32_t pk[32];
-        float sum = 0.f;
-#pragma unroll
-        for (int q = 0; q < 32; ++q) {
-          const uint32_t* src = q < 16 ? sa : sb;
-          const int qq = (q & 15) * 2;
-          // masked rows hold -inf: fma gives -inf, ex2 gives 0
-          const float p0 = none ? 0.f : ex2(fmaf(__uint_as_float(src[qq]), c, neg_m));
-          const float p1 = none ? 0.f : ex2(fmaf(__uint_as_float(src[qq + 1]), c, neg_m));
-          pk[q] = pack_f16x2(p0, p1);
-          sum += p0 + p1;
-        }
-        l += sum;
         // stage P + rescale factor + flags; slot u & 1 of the staging area
         const int st = u & 1;
         const uint32_t stage = sbase + L::kPStage + st * L::kPStageStride;
         if (tid == 0) bulk_wait_read<1>();  // the copy that last used this slot has read it
-        group_sync();
+        ok = group_and(ok);                 // (also carries thread 0's last send status)
+        if (!ok) break;
+        // P = 2^(s c - m_ref) in two halves of 32 rows; masked rows hold -inf
+        // (fma gives -inf, ex2 gives 0). Pairs go through the packed fp32 ops.
+        const uint64_t c2 = f32x2(c, c), nm2 = f32x2(neg_m, neg_m);
+        uint64_t sum2 = f32x2(0.f, 0.f);
+        auto p_half = [&](const uint32_t (&x)[32], int hx) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc)
-          st_shared_v4(stage + sw128_off(h, cc), pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2],
-                       pk[4 * cc + 3]);
+          for (int q = 0; q < 16; ++q) {
+            float t0, t1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(x[2 * q]), __uint_as_float(x[2 * q + 1])),
+                                  c2, nm2),
+                        t0, t1);
+            const float p0 = none ? 0.f : ex2(t0);
+            const float p1 = none ? 0.f : ex2(t1);
+            pk[q] = pack_f16x2(p0, p1);
+            sum2 = add_f32x2(sum2, f32x2(p0, p1));
+          }
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc)
+            st_shared_v4(stage + sw128_off(h, 4 * hx + cc), pk[4 * cc], pk[4 * cc + 1],
+                         pk[4 * cc + 2], pk[4 * cc + 3]);
+        };
+        p_half(sa, 0);
+        p_half(sb, 1);
+        float sum_lo, sum_hi;
+        f32x2_split(sum2, sum_lo, sum_hi);
+        l += sum_lo + sum_hi;
         st_shared_u32(stage + 16384 + 4 * h, __float_as_uint(alpha));
         const bool warp_resc = __any_sync(0xffffffffu, resc && u > 0);
         if (lane == 0) st_shared_u32(stage + 16384 + 512 + 4 * warp, warp_resc ? 1u : 0u);
         fence_proxy_async_cta();  // generic stores -> visible to the bulk copy
-        bool sent = true;
+        group_sync();             // every thread's part of P is staged
+        // Thread 0 alone waits for the peer's buffer and sends; the others go
+        // on with the next sub-tile and meet it at that sub-tile's staging.
         if (tid == 0) {
           // the peer's P buffer st is free once its P V of sub-tile u-2 completed
-          sent = wait_bar(bar(Ctl::kPEmpty, st), ((u >> 1) & 1u) ^ 1u, abort_addr);
-        }
-        ok = group_and(sent);
-        if (!ok) break;
-        if (tid == 0) {
-          const uint32_t pbar = peer_ctl + Ctl::kPFull + 8 * st;
-          mbar_arrive_tx_cluster(pbar, 16384 + kAFBytes);
-          bulk_s2s(peer_p + st * L::kPTile, stage, 16384, pbar);
-          bulk_s2s(peer_ctl + Ctl::kAF + st * kAFBytes, stage + 16384, kAFBytes, pbar);
-          bulk_commit();
+          ok = wait_bar(bar(Ctl::kPEmpty, st), ((u >> 1) & 1u) ^ 1u, abort_addr);
+          if (ok) {
+            const uint32_t pbar = peer_ctl + Ctl::kPFull + 8 * st;
+            mbar_arrive_tx_cluster(pbar, 16384 + kAFBytes);
+            bulk_s2s(peer_p + st * L::kPTile, stage, 16384, pbar);
+            bulk_s2s(peer_ctl + Ctl::kAF + st * kAFBytes, stage + 16384, kAFBytes, pbar);
+            bulk_commit();
+          }
         }
       }
     }
     if (tid == 0) bulk_wait_read<0>();  // this CTA's staging is read before it exits
+    ok = group_and(ok);
     if (ok) {
       st_cluster_u32(peer_ctl + Ctl::kFinalM + 4 * h, __float_as_uint(m_ref));
       st_cluster_u32(peer_ctl + Ctl::kFinalL + 4 * h, __float_as_uint(l));
