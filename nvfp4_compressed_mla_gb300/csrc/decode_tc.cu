@@ -34,13 +34,17 @@
 // top-k slots through the block table (-1 and unresolvable slots issue no
 // load), batching the index and block-table loads four stages ahead, and
 // publishes per 64-slot stage the rows' byte offsets and a live-row mask.
-// Eight dequant warps issue one bulk copy per live row into a ring of
-// stages (the stage's mbarrier expects live rows x row bytes), then expand
-// E2M1 x E4M3 (exact in FP16) into the 128-byte-swizzled layouts the MMAs
-// read (K-major K chunks in the score CTA, MN-major V slots in the output
-// CTA). One thread issues the MMAs; commits signal mbarriers. Softmax:
-// P = 2^(s - m_ref) with m_ref raised only when a score exceeds it by more
-// than 8 (so P <= 256 in FP16) and O rescaled only on those (rare) tiles.
+// Two copy warps gather the live rows with tile::gather4 tensor copies (four
+// rows per copy; one bulk copy per row when the page stride is not a whole
+// number of rows) into rows padded to an odd number of 16-byte units, so
+// eight consecutive rows hit distinct bank groups. Eight dequant warps then
+// expand E2M1 x E4M3 (exact in FP16) into the 128-byte-swizzled layouts the
+// MMAs read (K-major K chunks in the score CTA, MN-major V slots in the
+// output CTA). One thread issues the MMAs; commits signal mbarriers. The
+// MMA warp shares its SM sub-partition with the two copy warps rather than
+// with dequant warps. Softmax: P = 2^(s - m_ref) with m_ref raised only when
+// a score exceeds it by more than 8 (so P <= 256 in FP16) and O rescaled
+// only on those (rare) tiles.
 //
 // Every wait is bounded (about a second of clock64 cycles); a wait that
 // runs out sets an abort flag, the roles unwind together, tensor memory is
@@ -61,8 +65,15 @@ constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
 constexpr int kProducerWarp = 4;
 constexpr int kMmaWarp = 5;
-constexpr int kDequantWarp0 = 6;     // warps 6-13: dequant
-constexpr int kIssueWarp0 = 14;      // warps 14-15: gather copies
+// Gather copies: warps 9 and 13; dequant: warps 6, 7, 8, 10, 11, 12, 14, 15.
+// Warp w runs on SM sub-partition w % 4; sub-partition 1 holds the MMA warp
+// with the two light copy warps (and one softmax / correction warp) so that
+// the single MMA-issuing thread does not compete with dequant warps.
+constexpr int kCopyWarpA = 9, kCopyWarpB = 13;
+__device__ __forceinline__ bool is_copy_warp(int w) { return w == kCopyWarpA || w == kCopyWarpB; }
+__device__ __forceinline__ int dequant_index(int w) {  // 0..7 for the dequant warps
+  return w - 6 - (w > kCopyWarpA ? 1 : 0) - (w > kCopyWarpB ? 1 : 0);
+}
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSCol = 256;      // score CTA: S buffers at columns 256 and 384
 constexpr int kChunkSlots = 4;
@@ -158,15 +169,28 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+// Phase test. Barriers that only this CTA's threads, copies and MMAs arrive
+// on are waited with CTA-scope acquire; cluster scope (a costlier fence) is
+// kept for the few that the peer CTA arrives on.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
@@ -395,22 +419,33 @@ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t chunk) {
 // try_wait with a suspend-time hint: a waiting thread sleeps until the phase
 // completes (or the hint expires) instead of spinning.
 constexpr uint32_t kSuspendNs = 20000;
+template <bool kCluster>
 __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kSuspendNs)
-      : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "r"(kSuspendNs)
+        : "memory");
   return ok != 0;
 }
+template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t abort_addr) {
-  if (mbar_test(bar, parity)) return true;
+  if (mbar_test<kCluster>(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_wait_suspend(bar, parity)) return true;
+    if (mbar_wait_suspend<kCluster>(bar, parity)) return true;
     if (ld_shared_u32(abort_addr) != 0) return false;
     if (clock64() - t0 > kWaitCycles) {
       st_shared_u32(abort_addr, 1u);
@@ -421,8 +456,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t
 
 // Warp-uniform bounded wait: every lane waits (and so acquires) and the
 // warp leaves together, so warp-collective operations after it stay converged.
+template <bool kCluster = false>
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, uint32_t abort_addr) {
-  return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_addr));
+  return __all_sync(0xffffffffu, wait_bar<kCluster>(bar, parity, abort_addr));
 }
 
 // Bounded wait that ignores the abort flag: drains issued MMAs before the
@@ -498,6 +534,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n_tiles = min(p.tiles_per_split, p.num_tiles - tile0);
   const int n_sub = 2 * n_tiles;
 
+  // The resolve warp's first global loads (sequence, length, the first four
+  // stages' top-k slots) go out before the set-up, so their latency overlaps it.
+  const int32_t b = __ldg(p.q_seq + t);
+  const int32_t len = (b >= 0 && b < p.num_seqs) ? __ldg(p.seq_lens + b) : 0;
+  const int32_t* idx_row = p.topk_idx + static_cast<int64_t>(t) * p.topk;
+  auto load_pos = [&](int u, int32_t (&pos)[2]) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int slot = tile0 * kTile + u * kSub + lane + 32 * j;
+      pos[j] = (u < n_sub && slot < p.topk) ? __ldg(idx_row + slot) : -1;
+    }
+  };
+  int32_t posa[4][2];
+  if (warp == kProducerWarp) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) load_pos(k, posa[k]);
+  }
+
   auto bar = [&](int off, int i) { return ctl + off + 8u * static_cast<uint32_t>(i); };
   const uint32_t abort_addr = ctl + Ctl::kAbort;
   const int stages = rank == 0 ? L::kStagesS : L::kStagesO;
@@ -542,24 +596,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (tmem != 0u && tid == 0) st_shared_u32(abort_addr, 1u);  // MMA operands assume base 0
 
   if (rank == 0) {
-    // Q of this token, issued first and spread over all warps (a copy
-    // instruction stalls its warp for a while): latent row r by warp r % 14,
-    // lane r / 14, into a 1040-byte pitch; the rope rows by one copy.
+    // Q of this token, issued first and spread over the 13 warps other than
+    // the resolve and copy warps (a copy instruction stalls its warp for a
+    // while): latent row r by lane r / 13 of the (r % 13)-th of them, into a
+    // 1040-byte pitch; the rope rows by one copy.
     const int H = p.num_heads;
     const uint32_t qbar = bar(Ctl::kQFull, 0);
     if (tid == 0) mbar_arrive_tx(qbar, static_cast<uint32_t>(H * (kLatent + kRope) * 2));
     __syncwarp();
     const uint16_t* qlat_t = p.q_lat + static_cast<int64_t>(t) * H * kLatent;
-    for (int r = lane * kWarps + warp; r < H && lane < 10; r += 32 * kWarps)
-      bulk_g2s(sbase + L::kQStage + r * L::kQPitch, qlat_t + static_cast<int64_t>(r) * kLatent,
-               kLatent * 2, qbar);
+    const int qw = warp - (warp > kProducerWarp ? 1 : 0) - (warp > kCopyWarpA ? 1 : 0) -
+                   (warp > kCopyWarpB ? 1 : 0);
+    if (warp != kProducerWarp && !is_copy_warp(warp))
+      for (int r = lane * 13 + qw; r < H && lane < 10; r += 32 * 13)
+        bulk_g2s(sbase + L::kQStage + r * L::kQPitch, qlat_t + static_cast<int64_t>(r) * kLatent,
+                 kLatent * 2, qbar);
     if (tid == 32)
       bulk_g2s(sbase + L::kQStage + L::kQRopeStage, p.q_rope + static_cast<int64_t>(t) * H * kRope,
                static_cast<uint32_t>(H * kRope * 2), qbar);
   }
-  const int32_t b = __ldg(p.q_seq + t);
-  const int32_t len = (b >= 0 && b < p.num_seqs) ? __ldg(p.seq_lens + b) : 0;
-  const int32_t* idx_row = p.topk_idx + static_cast<int64_t>(t) * p.topk;
+  // Score CTA start-up: Q latent (bf16 staging rows) -> FP16 in TMEM, the QK
+  // MMA's A operand, by the softmax warps (thread = head). Chunk c is 64 dims
+  // (32 TMEM columns) of one head.
+  auto convert_q = [&](int c0, int c1, bool live) {
+    const int h = warp * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    live = live && h < p.num_heads;
+#pragma unroll 1
+    for (int c = c0; c < c1; ++c) {
+      uint32_t r[32];
+      const uint32_t src = sbase + L::kQStage + h * L::kQPitch + c * 128;
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const uint4 x = bf16x8_to_f16x8(
+            live ? ld_shared_v4(src + v * 16) : make_uint4(0u, 0u, 0u, 0u), p.q_lat_mult);
+        r[4 * v] = x.x;
+        r[4 * v + 1] = x.y;
+        r[4 * v + 2] = x.z;
+        r[4 * v + 3] = x.w;
+      }
+      tmem_st32(tmem + lane_base + 32u * c, r);
+    }
+    tmem_st_wait();
+  };
   const uint32_t copy = rank == 0 ? L::kCopyS : L::kCopyO;
   const uint32_t raw_base = sbase + (rank == 0 ? L::kRawS : L::kRawO);
   const uint32_t stage_bytes = rank == 0 ? L::kStageS : L::kStageO;
@@ -619,11 +698,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     return true;
   };
 
-  if (warp >= kIssueWarp0) {
+  if (is_copy_warp(warp)) {
     // ------------------------------------------------ gather copies
     // (score CTA: Q is staged over the ring until it is converted)
     bool run = rank != 0 || warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);
-    for (int u = 0; u < n_sub && run; ++u) run = issue_stage(u, warp - kIssueWarp0);
+    for (int u = 0; u < n_sub && run; ++u) run = issue_stage(u, warp == kCopyWarpA ? 0 : 1);
   } else if (warp == kProducerWarp) {
     // ------------------------------------------------ resolve: slots -> row offsets
     // Index and block-table loads are dependent global loads; four stages are
@@ -631,31 +710,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // next batch's index loads overlap this batch's block-table loads.
     const bool seq_ok = b >= 0 && b < p.num_seqs;
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(seq_ok ? b : 0) * p.max_blocks;
-    auto load_pos = [&](int u, int32_t (&pos)[2]) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int slot = tile0 * kTile + u * kSub + lane + 32 * j;
-        pos[j] = (u < n_sub && slot < p.topk) ? __ldg(idx_row + slot) : -1;
-      }
-    };
-    // page of a position: >= 0, -1 for an empty slot, -2 when it does not resolve
+    // page of a position: >= 0, -1 for an empty slot, -2 when it does not
+    // resolve. The block-table load is issued before the length check (its
+    // index is kept inside the sequence's row), so it does not wait on the
+    // length load.
     auto load_page = [&](const int32_t (&pos)[2], int64_t (&pg)[2]) {
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
         const int32_t ps = pos[j];
-        if (ps == -1) {
-          pg[j] = -1;
-        } else if (!seq_ok || ps < 0 || ps >= len || ps / p.page_size >= p.max_blocks) {
-          pg[j] = -2;
-        } else {
-          const int64_t e = __ldg(bt_row + ps / p.page_size);
-          pg[j] = (e < 0 || e >= p.num_blocks) ? -2 : e;
-        }
+        const int32_t pi = ps >= 0 ? ps / p.page_size : -1;
+        const bool in_row = seq_ok && pi >= 0 && pi < p.max_blocks;
+        const int64_t e = in_row ? __ldg(bt_row + pi) : -1;
+        pg[j] = ps == -1 ? -1 : (!in_row || ps >= len || e < 0 || e >= p.num_blocks) ? -2 : e;
       }
     };
-    int32_t posa[4][2];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) load_pos(k, posa[k]);
     bool stop = false;
     for (int u0 = 0; u0 < n_sub && !stop; u0 += 4) {
       int64_t pg[4][2];
@@ -706,11 +774,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         posa[k][1] = posb[k][1];
       }
     }
-  } else if (warp >= kDequantWarp0 && rank == 0) {
+  } else if (warp >= 6 && rank == 0) {
     // ------------------------------------------------ score CTA: gather + K chunks
     // Chunk kb of tile i: rows 0..127 of the tile x dims [64 kb, 64 kb + 64)
     // (kb = 8: the 64 rope dims). Thread -> (row, half of the chunk's dims).
-    const int dt = tid - kDequantWarp0 * 32;
+    const int dt = dequant_index(warp) * 32 + lane;
     const int row = dt & 127;
     const int hf = dt >> 7;
     bool run = warp_wait(bar(Ctl::kQReady, 0), 0, abort_addr);  // Q staging overlaps the ring
@@ -807,12 +875,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(Ctl::kRawEmpty, sb));
       }
     }
-  } else if (warp >= kDequantWarp0) {
+  } else if (warp >= 6) {
     // ------------------------------------------------ output CTA: gather + V slots
     // V (rows x 512 dims, FP16) is read by the P V MMA MN-major: each 32-row
     // slot holds 8 blocks of 64 dims, each block 4 groups of 8 rows x 128 B.
     // Thread item = (row, 16-dim group); 4 items per thread per slot.
-    const int dt = tid - kDequantWarp0 * 32;
+    const int dt = dequant_index(warp) * 32 + lane;
     bool run = true;
     for (int u = 0; u < n_sub && run; ++u) {
       const int s = u % L::kStagesO;
@@ -926,7 +994,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int va = ha % L::kVSlots, vb = hb % L::kVSlots;
           if (!wait_bar(bar(Ctl::kVtFull, va), (ha / L::kVSlots) & 1u, abort_addr)) break;
           if (!wait_bar(bar(Ctl::kVtFull, vb), (hb / L::kVSlots) & 1u, abort_addr)) break;
-          if (!wait_bar(bar(Ctl::kPFull, s2), k2 & 1u, abort_addr)) break;
+          if (!wait_bar<true>(bar(Ctl::kPFull, s2), k2 & 1u, abort_addr)) break;
           const uint4 fl = ld_shared_v4(ctl + Ctl::kAF + s2 * kAFBytes + 512);
           if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
             if (!wait_bar(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr)) break;
@@ -968,28 +1036,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t rope_at = sbase + L::kQStage + L::kQRopeStage;
       ok = group_and(wait_bar(qbar, 0, abort_addr));  // copies issued at set-up
       const bool live = ok && h < p.num_heads;
-#pragma unroll 1
-      for (int c = 0; c < 8; ++c) {
-        uint32_t r[32];
-        const uint32_t src = sbase + L::kQStage + h * L::kQPitch + c * 128;
-#pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = bf16x8_to_f16x8(
-              live ? ld_shared_v4(src + v * 16) : make_uint4(0u, 0u, 0u, 0u), p.q_lat_mult);
-          r[4 * v] = x.x;
-          r[4 * v + 1] = x.y;
-          r[4 * v + 2] = x.z;
-          r[4 * v + 3] = x.w;
-        }
-        tmem_st32(tmem + lane_base + 32u * c, r);
-      }
+      convert_q(0, 8, ok);
       uint4 qr[8];
 #pragma unroll
       for (int v = 0; v < 8; ++v)
         qr[v] = bf16x8_to_f16x8(live ? ld_shared_v4(rope_at + h * (kRope * 2) + v * 16)
                                      : make_uint4(0u, 0u, 0u, 0u),
                                 p.q_rope_mult);
-      tmem_st_wait();
+      __syncwarp();
       group_sync();  // every staged row has been read: the rope operand may overwrite it
 #pragma unroll
       for (int v = 0; v < 8; ++v)
@@ -1098,7 +1152,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // on with the next sub-tile and meet it at that sub-tile's staging.
         if (tid == 0) {
           // the peer's P buffer st is free once its P V of sub-tile u-2 completed
-          ok = wait_bar(bar(Ctl::kPEmpty, st), ((u >> 1) & 1u) ^ 1u, abort_addr);
+          ok = wait_bar<true>(bar(Ctl::kPEmpty, st), ((u >> 1) & 1u) ^ 1u, abort_addr);
           if (ok) {
             const uint32_t pbar = peer_ctl + Ctl::kPFull + 8 * st;
             mbar_arrive_tx_cluster(pbar, 16384 + kAFBytes);
@@ -1139,7 +1193,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (u + 1 < n_sub) {
         const int n2 = (u + 1) & 1;
         const uint32_t nk2 = (u + 1) >> 1;
-        if (!warp_wait(bar(Ctl::kPFull, n2), nk2 & 1u, abort_addr)) {
+        if (!warp_wait<true>(bar(Ctl::kPFull, n2), nk2 & 1u, abort_addr)) {
           ok = false;
           break;
         }
@@ -1164,7 +1218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     float m_fin = NAN, l_fin = 0.f;
     ok = __all_sync(0xffffffffu, ok);
-    if (ok && warp_wait(bar(Ctl::kStats, 0), 0, abort_addr)) {
+    if (ok && warp_wait<true>(bar(Ctl::kStats, 0), 0, abort_addr)) {
       m_fin = __uint_as_float(ld_shared_u32(ctl + Ctl::kFinalM + 4 * h));
       l_fin = __uint_as_float(ld_shared_u32(ctl + Ctl::kFinalL + 4 * h));
     } else {
