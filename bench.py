@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--sweep", action="store_true",
+                    help="head sweep (16/32/64/128 heads on decode_batch) and the 15 query "
+                         "tokens x 16 heads x top-2048 point; one JSON line per point")
     return ap.parse_args()
 
 
@@ -458,6 +461,135 @@ def traffic_from_profiles(fmt, config):
     return d["per_launch_bytes"][key]
 
 
+def run_sweep(args):
+    """Decode µs/launch over a head sweep and at 15 query tokens x 16 heads x top-2048.
+
+    Each point is timed as a CUDA graph of 100 decode launches that walk
+    through enough layer caches (own pool rows, queries, top-k) that the
+    rotation's selected rows exceed 4 x the 129 MB L2; the graph is replayed
+    after 20 warm-up launches and the median of 5 replays is reported. If the
+    capture fails, the same launches are timed back to back on the stream
+    and the line says so. One JSON line per point.
+    """
+    import torch
+
+    import nvfp4_compressed_mla_gb300 as nm
+    from nvfp4_compressed_mla_gb300 import _native
+    from workloads import all_tokens, make_workload, redraw_indices
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    lib = _native.load()
+    peaks = load_peaks()
+    fmt = args.row_format
+    stride = 64 * ROW_BYTES[fmt]
+    points = [("decode_batch", {"num_heads": h}) for h in (16, 32, 64, 128)]
+    points.append(("multi_token", {"num_seqs": 1, "q_per_seq": 15, "num_heads": 16}))
+    g = torch.Generator(device=dev)
+    pools = {}
+    n_launch, n_warm, n_rep = 100, 20, 5
+    for name, kw in points:
+        wl = make_workload(name, **kw)
+        alg = algorithmic(wl, fmt)
+        pool_bytes = wl.num_blocks * stride
+        layers = max(2, min(64, math.ceil(4 * 129e6 / max(alg["kv_bytes"], 1)) + 1))
+        key = (name, kw.get("num_seqs"))
+        have = pools.get(key, [])
+        free, _ = torch.cuda.mem_get_info(dev)
+        layers = max(1, min(layers, len(have) + int(0.5 * free // max(pool_bytes, 1))))
+        if len(have) < layers:  # pools do not depend on the head count: fill once, reuse
+            all_seq, all_pos = all_tokens(wl)
+            sd = torch.from_numpy(all_seq).to(dev)
+            pd = torch.from_numpy(all_pos).to(dev)
+            bt0 = torch.from_numpy(wl.block_table).to(dev)
+            for li in range(len(have), layers):
+                g.manual_seed(777 + li)
+                pool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
+                for s0 in range(0, all_seq.size, 1 << 20):
+                    e0 = min(s0 + (1 << 20), all_seq.size)
+                    lat = torch.randn((e0 - s0, 512), generator=g, device=dev).to(torch.bfloat16)
+                    rope = torch.randn((e0 - s0, 64), generator=g, device=dev).to(torch.bfloat16)
+                    nm.nvfp4_mla_append(lat, rope, sd[s0:e0], pd[s0:e0], bt0, 64, pool,
+                                        wl.num_blocks, stride, fmt)
+                have.append(pool)
+            pools[key] = have
+        bt = torch.from_numpy(wl.block_table).to(dev)
+        seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
+        q_seq = torch.from_numpy(wl.q_seq).to(dev)
+        H = wl.num_heads
+        per = []
+        for li in range(layers):
+            idx = wl.topk_idx if li == 0 else redraw_indices(wl, li)
+            per.append(dict(
+                ql=torch.randn((wl.num_q, H, 512), generator=g, device=dev).to(torch.bfloat16),
+                qr=torch.randn((wl.num_q, H, 64), generator=g, device=dev).to(torch.bfloat16),
+                idx=torch.from_numpy(np.ascontiguousarray(idx)).to(dev)))
+        out = torch.empty((wl.num_q, H, 512), dtype=torch.bfloat16, device=dev)
+        lse = torch.empty((wl.num_q, H), dtype=torch.float32, device=dev)
+        splits = lib.sparse_mla_decode_num_splits(wl.num_q, H, wl.topk)
+        ws_bytes = nm.sparse_mla_decode_workspace_size(wl.num_q, H, wl.topk, splits)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        cap = torch.cuda.Stream(dev)
+
+        def dec_args(li, sh):
+            d = per[li]
+            return (d["ql"].data_ptr(), d["qr"].data_ptr(), q_seq.data_ptr(), d["idx"].data_ptr(),
+                    wl.num_q, H, wl.topk, bt.data_ptr(), wl.num_seqs, wl.max_blocks_per_seq,
+                    seq_lens.data_ptr(), 64, have[li].data_ptr(), wl.num_blocks, stride, fmt,
+                    wl.sm_scale, 1.0, 1.0, out.data_ptr(), 0, lse.data_ptr(), ws.data_ptr(),
+                    ws.numel(), splits, None, sh)
+
+        args_cap = [dec_args(i % layers, cap.cuda_stream) for i in range(n_launch)]
+        with torch.cuda.stream(cap):
+            for i in range(n_warm):
+                if lib.sparse_mla_decode(*args_cap[i % n_launch]):
+                    raise RuntimeError("decode failed")
+        torch.cuda.synchronize()
+        timing = "cuda graph of 100 launches, median of 5 replays"
+        times = []
+        try:
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=cap):
+                for a in args_cap:
+                    if lib.sparse_mla_decode(*a):
+                        raise RuntimeError("a decode launch failed during capture")
+            graph.replay()
+            torch.cuda.synchronize()
+            for _ in range(n_rep):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(cap)
+                with torch.cuda.stream(cap):
+                    graph.replay()
+                e1.record(cap)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+        except RuntimeError as exc:  # capture refused: time the same launches eagerly
+            torch.cuda.synchronize()
+            timing = f"eager launches (graph capture failed: {str(exc).splitlines()[0][:80]})"
+            times = []
+            for _ in range(n_rep):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(cap)
+                for a in args_cap:
+                    lib.sparse_mla_decode(*a)
+                e1.record(cap)
+                torch.cuda.synchronize()
+                times.append(e0.elapsed_time(e1))
+        us = float(np.median(times)) * 1e3 / n_launch
+        t = us * 1e-6
+        cfg = describe(wl, fmt)
+        cfg.update({"layers_rotated": layers, "num_splits": splits, "timing": timing})
+        print(json.dumps({
+            "sweep_point": f"{wl.num_q} q x {H} heads x top-{wl.topk}",
+            "us_per_launch": round(us, 3),
+            "kv_gbs": round(alg["kv_bytes"] / t / 1e9, 1),
+            "hbm_frac": round(alg["bytes"] / t / 1e9 / peaks["hbm_gbs"], 4),
+            "tensor_frac": round(alg["flops"] / t / 1e12 / peaks["bf16_tflops"], 4),
+            "config": cfg}), flush=True)
+        del per, out, lse, ws
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -466,6 +598,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.sweep:
+        if rank == 0:
+            run_sweep(args)
         return
     if world > 1:
         import torch
