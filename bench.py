@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--staged", action="store_true",
+                    help="fused decode vs the staged comparison path (selected rows to an FP8 "
+                         "buffer, then the FP8 decode) on --config; one JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="head sweep (16/32/64/128 heads on decode_batch) and the 15 query "
                          "tokens x 16 heads x top-2048 point; one JSON line per point")
@@ -461,6 +464,138 @@ def traffic_from_profiles(fmt, config):
     return d["per_launch_bytes"][key]
 
 
+def run_staged(args):
+    """Fused NVFP4 decode vs the staged comparison path on the same inputs.
+
+    The staged path is nvfp4_mla_stage_fp8 (selected rows re-encoded as FP8
+    rows in a device buffer) followed by sparse_mla_decode over that buffer
+    with FP8 rows. Both are timed as CUDA graphs of 100 steps over rotated
+    layer caches (median of 5 replays after 20 warm-up steps).
+    """
+    import torch
+
+    import nvfp4_compressed_mla_gb300 as nm
+    from nvfp4_compressed_mla_gb300 import _native
+    from workloads import all_tokens, make_workload, redraw_indices
+
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    lib = _native.load()
+    peaks = load_peaks()
+    wl = make_workload(args.config)
+    stride = 64 * ROW_BYTES[0]
+    alg = algorithmic(wl, 0)
+    pool_bytes = wl.num_blocks * stride
+    layers = args.layers or max(2, min(16, math.ceil(4 * 129e6 / max(alg["kv_bytes"], 1)) + 1))
+    free, _ = torch.cuda.mem_get_info(dev)
+    layers = max(1, min(layers, int(0.5 * free // max(pool_bytes, 1))))
+    g = torch.Generator(device=dev)
+    bt = torch.from_numpy(wl.block_table).to(dev)
+    seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
+    q_seq = torch.from_numpy(wl.q_seq).to(dev)
+    all_seq, all_pos = all_tokens(wl)
+    sd = torch.from_numpy(all_seq).to(dev)
+    pd = torch.from_numpy(all_pos).to(dev)
+    L = []
+    for li in range(layers):
+        g.manual_seed(4242 + li)
+        pool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
+        for s0 in range(0, all_seq.size, 1 << 20):
+            e0 = min(s0 + (1 << 20), all_seq.size)
+            lat = torch.randn((e0 - s0, 512), generator=g, device=dev).to(torch.bfloat16)
+            rope = torch.randn((e0 - s0, 64), generator=g, device=dev).to(torch.bfloat16)
+            nm.nvfp4_mla_append(lat, rope, sd[s0:e0], pd[s0:e0], bt, 64, pool, wl.num_blocks,
+                                stride, 0)
+        idx = wl.topk_idx if li == 0 else redraw_indices(wl, li)
+        L.append(dict(pool=pool,
+                      ql=torch.randn((wl.num_q, wl.num_heads, 512), generator=g,
+                                     device=dev).to(torch.bfloat16),
+                      qr=torch.randn((wl.num_q, wl.num_heads, 64), generator=g,
+                                     device=dev).to(torch.bfloat16),
+                      idx=torch.from_numpy(np.ascontiguousarray(idx)).to(dev)))
+    H, topk = wl.num_heads, wl.topk
+    out = torch.empty((wl.num_q, H, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.num_q, H), dtype=torch.float32, device=dev)
+    splits = lib.sparse_mla_decode_num_splits(wl.num_q, H, topk)
+    ws = torch.empty(max(nm.sparse_mla_decode_workspace_size(wl.num_q, H, topk, splits), 16),
+                     dtype=torch.uint8, device=dev)
+    R = nm.nvfp4_mla_staged_rows_per_q(topk, 64)
+    staged = torch.empty(wl.num_q * R * 576, dtype=torch.uint8, device=dev)
+    sidx = torch.empty((wl.num_q, topk), dtype=torch.int32, device=dev)
+    tb = nm.staged_fp8_tables(wl.num_q, topk, 64, dev)
+    cap = torch.cuda.Stream(dev)
+    sh = cap.cuda_stream
+
+    def fused(li):
+        d = L[li]
+        return lib.sparse_mla_decode(
+            d["ql"].data_ptr(), d["qr"].data_ptr(), q_seq.data_ptr(), d["idx"].data_ptr(),
+            wl.num_q, H, topk, bt.data_ptr(), wl.num_seqs, wl.max_blocks_per_seq,
+            seq_lens.data_ptr(), 64, d["pool"].data_ptr(), wl.num_blocks, stride, 0, wl.sm_scale,
+            1.0, 1.0, out.data_ptr(), 0, lse.data_ptr(), ws.data_ptr(), ws.numel(), splits,
+            None, sh)
+
+    def stage(li):
+        d = L[li]
+        return lib.nvfp4_mla_stage_fp8(
+            q_seq.data_ptr(), d["idx"].data_ptr(), wl.num_q, topk, bt.data_ptr(), wl.num_seqs,
+            wl.max_blocks_per_seq, seq_lens.data_ptr(), 64, d["pool"].data_ptr(), wl.num_blocks,
+            stride, 1.0, staged.data_ptr(), sidx.data_ptr(), None, sh)
+
+    def staged_decode(li):
+        d = L[li]
+        return lib.sparse_mla_decode(
+            d["ql"].data_ptr(), d["qr"].data_ptr(), tb["q_seq"].data_ptr(), sidx.data_ptr(),
+            wl.num_q, H, topk, tb["block_table"].data_ptr(), wl.num_q, R // 64,
+            tb["seq_lens"].data_ptr(), 64, staged.data_ptr(), tb["num_blocks"],
+            tb["block_stride_bytes"], 1, wl.sm_scale, 1.0, 1.0, out.data_ptr(), 0,
+            lse.data_ptr(), ws.data_ptr(), ws.numel(), splits, None, sh)
+
+    def timed(fns):
+        with torch.cuda.stream(cap):
+            for i in range(20):
+                for f in fns:
+                    if f(i % layers):
+                        raise RuntimeError("launch failed")
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=cap):
+            for i in range(100):
+                for f in fns:
+                    if f(i % layers):
+                        raise RuntimeError("launch failed during capture")
+        graph.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(cap)
+            with torch.cuda.stream(cap):
+                graph.replay()
+            e1.record(cap)
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts)) * 1e3 / 100
+
+    t_fused = timed([fused])
+    t_stage = timed([stage])
+    t_staged = timed([stage, staged_decode])
+    rows = wl.valid_slots()
+    cfg = describe(wl, 0)
+    cfg.update({"layers_rotated": layers, "num_splits": splits,
+                "timing": "cuda graphs of 100 steps, median of 5 replays"})
+    print(json.dumps({
+        "comparison": "fused NVFP4 decode vs staged (selected rows -> FP8 buffer -> FP8 decode)",
+        "fused_us": round(t_fused, 3),
+        "staged_us": round(t_staged, 3),
+        "stage_kernel_us": round(t_stage, 3),
+        "staged_over_fused": round(t_staged / t_fused, 3),
+        "stage_kernel_hbm_gbs": round(rows * (352 + 576) / (t_stage * 1e-6) / 1e9, 1),
+        "stage_kernel_hbm_frac": round(rows * (352 + 576) / (t_stage * 1e-6) / 1e9
+                                       / peaks["hbm_gbs"], 4),
+        "config": cfg}), flush=True)
+
+
 def run_sweep(args):
     """Decode µs/launch over a head sweep and at 15 query tokens x 16 heads x top-2048.
 
@@ -602,6 +737,10 @@ def main():
     if args.sweep:
         if rank == 0:
             run_sweep(args)
+        return
+    if args.staged:
+        if rank == 0:
+            run_staged(args)
         return
     if world > 1:
         import torch

@@ -215,6 +215,52 @@ int32_t sparse_mla_decode_noalloc(const void* q_latent, const void* q_rope, cons
                                   int32_t out_fp32, float* lse, int32_t num_splits,
                                   int32_t* invalid_count, void* stream);
 
+/*
+ * The staged-dequant comparison path of section "Native NVFP4 sparse MLA
+ * decode kernel": the post measures its fused kernel against a variant that
+ * first dequantises the selected rows into an FP8 temporary buffer in device
+ * memory and then runs the attention over that buffer. These two entry
+ * points build that buffer from an NVFP4 cache, so sparse_mla_decode with
+ * row_format NVFP4_MLA_ROW_FP8_576 can be run over it and the two paths
+ * timed on the same inputs. Not part of the fused decode.
+ *
+ * nvfp4_mla_staged_rows_per_q: staged rows per query token, topk rounded up
+ * to a multiple of page_size (each token's rows start a page); 0 for an
+ * invalid topk (outside 1..65536) or page_size (outside 1..2^20).
+ *
+ * nvfp4_mla_stage_fp8: for query token t and slot j of topk_idx[t] that
+ * resolves as in sparse_mla_decode (same rules, same invalid_count), the
+ * NVFP4 row is decoded (E2M1 code x E4M3 block scale, exact in fp32) and
+ * re-encoded as an FP8 row: latent byte = E4M3(fp32(value / latent_scale)),
+ * nearest with ties to even, saturating to +-448; the 64 rope bytes are
+ * copied (both formats store E4M3(rope / rope_scale)). The row is written
+ * to staged row t * R + j (R = nvfp4_mla_staged_rows_per_q(topk,
+ * page_size)) and staged_idx[t * topk + j] = j; a slot that does not
+ * resolve gets staged_idx = -1 and its staged row is left untouched.
+ *
+ *   q_seq .. block_stride_bytes  as for sparse_mla_decode, with an NVFP4 cache
+ *   latent_scale  finite, > 0: the FP8 rows' latent divisor
+ *   staged        device, 16-byte aligned, num_q * R * 576 bytes: the
+ *                 staged rows, contiguous
+ *   staged_idx    device int32 [num_q, topk]
+ *   invalid_count nullable device int32 (accumulated with atomicAdd)
+ *
+ * Reading the staged rows back with sparse_mla_decode: row_format FP8,
+ * the same latent_scale and rope_scale, cache = staged, page_size as here,
+ * block_stride_bytes = page_size * 576, num_blocks = num_q * R / page_size,
+ * num_seqs = num_q, max_blocks_per_seq = R / page_size, q_seq[t] = t,
+ * block_table[t][k] = t * (R / page_size) + k, seq_lens[t] = topk,
+ * topk_idx = staged_idx.
+ */
+int64_t nvfp4_mla_staged_rows_per_q(int32_t topk, int32_t page_size);
+
+int32_t nvfp4_mla_stage_fp8(const int32_t* q_seq, const int32_t* topk_idx, int32_t num_q,
+                            int32_t topk, const int32_t* block_table, int32_t num_seqs,
+                            int32_t max_blocks_per_seq, const int32_t* seq_lens,
+                            int32_t page_size, const void* cache, int64_t num_blocks,
+                            int64_t block_stride_bytes, float latent_scale, void* staged,
+                            int32_t* staged_idx, int32_t* invalid_count, void* stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -28,7 +28,7 @@ __all__ = [
     "LATENT_DIM", "ROPE_DIM", "ROW_NVFP4_352", "ROW_FP8_576", "ROW_BYTES", "NativeError",
     "nvfp4_mla_row_bytes", "nvfp4_mla_status_string", "nvfp4_mla_append",
     "sparse_mla_decode_num_splits", "sparse_mla_decode_workspace_size", "sparse_mla_decode",
-    "library_path",
+    "nvfp4_mla_staged_rows_per_q", "nvfp4_mla_stage_fp8", "staged_fp8_tables", "library_path",
 ]
 
 
@@ -136,3 +136,54 @@ def sparse_mla_decode(q_latent: torch.Tensor, q_rope: torch.Tensor, q_seq: torch
         num_splits, _ptr(invalid_count), _stream(stream))
     _check(st, "sparse_mla_decode")
     return out, lse
+
+
+# ------------------------------------------------ staged-dequant comparison path
+def nvfp4_mla_staged_rows_per_q(topk: int, page_size: int) -> int:
+    """Staged FP8 rows per query token (topk rounded up to whole pages)."""
+    n = int(_lib().nvfp4_mla_staged_rows_per_q(topk, page_size))
+    if n == 0:
+        raise ValueError("invalid topk or page_size")
+    return n
+
+
+def nvfp4_mla_stage_fp8(q_seq: torch.Tensor, topk_idx: torch.Tensor, block_table: torch.Tensor,
+                        seq_lens: torch.Tensor, page_size: int, cache: torch.Tensor,
+                        num_blocks: int, block_stride_bytes: int, latent_scale: float = 1.0,
+                        staged: Optional[torch.Tensor] = None,
+                        staged_idx: Optional[torch.Tensor] = None,
+                        invalid_count: Optional[torch.Tensor] = None, stream=None):
+    """Selected NVFP4 rows re-encoded as FP8 rows; returns (staged, staged_idx).
+
+    ``staged`` (uint8, num_q * R * 576 bytes) and ``staged_idx`` (int32
+    [num_q, topk]) are allocated with torch when not given.
+    """
+    num_q, topk = topk_idx.shape[0], topk_idx.shape[1]
+    dev = topk_idx.device
+    R = nvfp4_mla_staged_rows_per_q(topk, page_size)
+    if staged is None:
+        staged = torch.empty(max(num_q * R * ROW_BYTES[ROW_FP8_576], 16), dtype=torch.uint8,
+                             device=dev)
+    if staged_idx is None:
+        staged_idx = torch.empty((num_q, topk), dtype=torch.int32, device=dev)
+    st = _lib().nvfp4_mla_stage_fp8(
+        _ptr(q_seq), _ptr(topk_idx), num_q, topk, _ptr(block_table), block_table.shape[0],
+        block_table.shape[1], _ptr(seq_lens), page_size, _ptr(cache), num_blocks,
+        block_stride_bytes, latent_scale, _ptr(staged), _ptr(staged_idx), _ptr(invalid_count),
+        _stream(stream))
+    _check(st, "nvfp4_mla_stage_fp8")
+    return staged, staged_idx
+
+
+def staged_fp8_tables(num_q: int, topk: int, page_size: int, device) -> dict:
+    """Index tables for reading the staged rows with sparse_mla_decode (FP8 rows):
+    token t is sequence t, its rows fill pages t * P .. t * P + P - 1."""
+    R = nvfp4_mla_staged_rows_per_q(topk, page_size)
+    P = R // page_size
+    return {
+        "q_seq": torch.arange(num_q, dtype=torch.int32, device=device),
+        "block_table": torch.arange(num_q * P, dtype=torch.int32, device=device).view(num_q, P),
+        "seq_lens": torch.full((num_q,), topk, dtype=torch.int32, device=device),
+        "num_blocks": num_q * P,
+        "block_stride_bytes": page_size * ROW_BYTES[ROW_FP8_576],
+    }

@@ -73,6 +73,9 @@ def _load():
                                                   ctypes.c_int]
             lib.orc_sparse_mla_decode.restype = i64
             lib.orc_max_threads.restype = ctypes.c_int
+            lib.orc_stage_fp8.argtypes = [P, P, i32, i32, P, i32, i32, P, i32, P, i64, i64, f32,
+                                          i64, P, P]
+            lib.orc_stage_fp8.restype = i64
             _lib = lib
     return _lib
 
@@ -187,3 +190,26 @@ def sparse_mla_decode(q_latent_bf16, q_rope_bf16, q_seq, topk_idx, block_table, 
         block_stride, row_format, sm_scale, latent_scale, rope_scale, _ptr(out), _ptr(lse),
         nthreads)
     return out, lse, int(bad)
+
+
+# ------------------------------------------------------ staged FP8 rows
+def stage_fp8(q_seq, topk_idx, block_table, seq_lens, page_size: int, cache: np.ndarray,
+              num_blocks: int, block_stride: int, latent_scale: float = 1.0):
+    """Selected NVFP4 rows re-encoded as FP8 rows (the staged comparison path).
+
+    Returns (staged [num_q * R, 576] uint8, staged_idx [num_q, topk] int32,
+    invalid) with R = topk rounded up to a multiple of page_size; rows of
+    slots that do not resolve are zero.
+    """
+    q_seq = _c(q_seq, np.int32)
+    idx = _c(topk_idx, np.int32)
+    num_q, topk = idx.shape
+    bt = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    R = (topk + page_size - 1) // page_size * page_size
+    staged = np.zeros((num_q * R, ROW_BYTES[1]), np.uint8)
+    sidx = np.empty((num_q, topk), np.int32)
+    bad = _load().orc_stage_fp8(_ptr(q_seq), _ptr(idx), num_q, topk, _ptr(bt), bt.shape[0],
+                                bt.shape[1], _ptr(seq_lens), page_size, _ptr(cache), num_blocks,
+                                block_stride, latent_scale, R, _ptr(staged), _ptr(sidx))
+    return staged, sidx, int(bad)

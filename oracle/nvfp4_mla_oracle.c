@@ -284,6 +284,48 @@ int64_t orc_sparse_mla_decode(const uint16_t* q_lat, const uint16_t* q_rope, con
   return bad;
 }
 
+/* Staged-dequant comparison path (section "Native NVFP4 sparse MLA decode
+ * kernel": the post times its fused kernel against dequantising the selected
+ * rows into an FP8 temporary buffer first). For query token t and slot j
+ * that resolves in an NVFP4 cache, the row's latent values (code x block
+ * scale, exact) are re-encoded as E4M3 of the fp32 quotient value /
+ * latent_scale (nearest, ties to even, saturating), the rope bytes copied,
+ * and the 576-byte row stored as staged row t * rows_per_q + j with
+ * staged_idx = j. Slots that do not resolve get staged_idx = -1; those
+ * other than -1 are counted (returned). */
+int64_t orc_stage_fp8(const int32_t* q_seq, const int32_t* topk_idx, int32_t num_q, int32_t topk,
+                      const int32_t* block_table, int32_t num_seqs, int32_t max_blocks,
+                      const int32_t* seq_lens, int32_t page_size, const uint8_t* cache,
+                      int64_t num_blocks, int64_t block_stride, float latent_scale,
+                      int64_t rows_per_q, uint8_t* staged, int32_t* staged_idx) {
+  int64_t bad = 0;
+  double lat[ORC_LATENT], rope[ORC_ROPE];
+  for (int32_t t = 0; t < num_q; ++t) {
+    int32_t b = q_seq[t];
+    int32_t len = (b >= 0 && b < num_seqs) ? seq_lens[b] : 0;
+    for (int32_t j = 0; j < topk; ++j) {
+      int32_t pos = topk_idx[(int64_t)t * topk + j];
+      int64_t off = pos == -1 ? -1
+                              : resolve(b, pos, len, block_table, num_seqs, max_blocks, page_size,
+                                        num_blocks, block_stride, ORC_NVFP4_ROW);
+      staged_idx[(int64_t)t * topk + j] = off >= 0 ? j : -1;
+      if (off < 0) {
+        if (pos != -1) ++bad;
+        continue;
+      }
+      const uint8_t* row = cache + off;
+      uint8_t* dst = staged + ((int64_t)t * rows_per_q + j) * ORC_FP8_ROW;
+      orc_dequant_row(row, 0, 1.0f, 1.0f, lat, rope);
+      for (int k = 0; k < ORC_LATENT; ++k) {
+        float q = (float)lat[k] / latent_scale; /* value exact in fp32; quotient IEEE rounded */
+        dst[k] = orc_e4m3_encode((double)q);
+      }
+      for (int k = 0; k < ORC_ROPE; ++k) dst[ORC_LATENT + k] = row[288 + k];
+    }
+  }
+  return bad;
+}
+
 int orc_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -413,3 +413,48 @@ def test_fp8_rows_attention_uses_scales():
     s = torch.from_numpy(wl.sm_scale * (Q @ L.T + QR @ R.T))
     want = torch.softmax(s, -1).numpy() @ L
     assert np.allclose(out[0], want, rtol=1e-12, atol=1e-13)
+
+
+# ------------------------------------------------------ staged FP8 rows
+def test_stage_fp8_matches_torch_reencoding_and_placement():
+    """Staged rows: torch's float8_e4m3fn of the fp32 quotient dequantised value /
+    latent_scale (values kept within +-448 here, where torch does not saturate),
+    rope bytes copied, row t * R + j, -1 and unresolvable slots marked -1."""
+    wl = make_workload("tiny", num_seqs=2, seq_len=300, num_heads=1, topk=70, q_per_seq=2)
+    from workloads import all_tokens
+    seq, pos = all_tokens(wl)
+    lat, rope = make_rows(wl, int(seq.size))
+    stride = 64 * 352
+    pool = np.zeros(wl.num_blocks * stride, np.uint8)
+    assert oracle.append(lat, rope, seq, pos, wl.block_table, 64, pool, wl.num_blocks,
+                         stride) == 0
+    idx = wl.topk_idx.copy()
+    idx[0, 3] = -1            # empty slot: not counted
+    idx[1, 5] = 10 ** 6       # beyond the sequence: counted
+    idx[2, 0] = -7            # negative: counted
+    ls = 0.375
+    staged, sidx, bad = oracle.stage_fp8(wl.q_seq, idx, wl.block_table, wl.seq_lens, 64, pool,
+                                         wl.num_blocks, stride, latent_scale=ls)
+    assert bad == 2
+    R = 128  # 70 rounded up to whole 64-row pages
+    assert staged.shape == (wl.num_q * R, 576)
+    n_checked = 0
+    for t in range(wl.num_q):
+        b = wl.q_seq[t]
+        for j in range(wl.topk):
+            p = idx[t, j]
+            ok = 0 <= p < wl.seq_lens[b]
+            assert sidx[t, j] == (j if ok else -1)
+            row_out = staged[t * R + j]
+            if not ok:
+                assert not row_out.any()
+                continue
+            page = wl.block_table[b, p // 64]
+            row_in = pool[page * stride + (p % 64) * 352:][:352]
+            vals, _ = oracle.dequant_rows(row_in[None], 0)
+            q = (vals[0].astype(np.float32) / np.float32(ls)).astype(np.float32)
+            assert np.all(np.abs(q) <= 448)
+            assert np.array_equal(row_out[:512], torch_e4m3(q))
+            assert np.array_equal(row_out[512:], row_in[288:])
+            n_checked += 1
+    assert n_checked == wl.num_q * wl.topk - 3
