@@ -46,6 +46,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--blhnc", action="store_true",
+                    help="one pool whose blocks hold every layer's page back to back "
+                         "(block stride = layers x page bytes) instead of one pool per layer")
     ap.add_argument("--staged", action="store_true",
                     help="fused decode vs the staged comparison path (selected rows to an FP8 "
                          "buffer, then the FP8 decode) on --config; one JSON line")
@@ -169,12 +172,17 @@ def run_ours(args, rank, world, local_rank):
                                           + 7919 * rank))
     fmt = args.row_format
     rb = ROW_BYTES[fmt]
-    stride = 64 * rb
-    pool_bytes = wl.num_blocks * stride
+    page_bytes = 64 * rb
+    pool_bytes = wl.num_blocks * page_bytes
     alg = algorithmic(wl, fmt)
     layers = args.layers or max(2, min(16, math.ceil(4 * 129e6 / max(alg["kv_bytes"], 1)) + 1))
     free, _ = torch.cuda.mem_get_info(dev)
     layers = max(1, min(layers, int(0.6 * free // max(pool_bytes, 1))))
+    # one pool per layer, or (BLHNC) one pool whose block b holds layer l's page at
+    # byte l * page_bytes: layer l is the pool from that offset with the wider stride
+    stride = layers * page_bytes if args.blhnc else page_bytes
+    shared_pool = (torch.empty(wl.num_blocks * stride, dtype=torch.uint8, device=dev)
+                   if args.blhnc else None)
 
     g = torch.Generator(device=dev)
     bt = torch.from_numpy(wl.block_table).to(dev)
@@ -205,7 +213,8 @@ def run_ours(args, rank, world, local_rank):
     L = []
     for li in range(layers):
         g.manual_seed(12345 + 1000 * rank + li)
-        pool = torch.empty(pool_bytes, dtype=torch.uint8, device=dev)
+        pool = (shared_pool[li * page_bytes:] if args.blhnc
+                else torch.empty(pool_bytes, dtype=torch.uint8, device=dev))
         chunk = 1 << 20
         for s in range(0, all_seq.size, chunk):
             e = min(s + chunk, all_seq.size)
@@ -779,7 +788,9 @@ def main():
                 "l2": f"inputs larger than L2: {res['layers']} layer caches rotated "
                       f"({res['layers'] - 1} x {alg['kv_bytes'] / 1e6:.1f} MB of other selected "
                       f"rows between reuses)",
-                "parallelism": f"replicas x{world}"})
+                "parallelism": f"replicas x{world}",
+                "cache_layout": ("BLHNC: one pool, each block holds every layer's 64-row page "
+                                 "back to back" if args.blhnc else "one pool per layer")})
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
