@@ -216,6 +216,29 @@ int32_t sparse_mla_decode_noalloc(const void* q_latent, const void* q_rope, cons
                                   int32_t* invalid_count, void* stream);
 
 /*
+ * Merge attention states computed over disjoint parts of each query token's
+ * top-k: the split-K merge of section "Native NVFP4 sparse MLA decode kernel"
+ * (there across the SMs of a cluster) for parts computed elsewhere, e.g. by
+ * the GPUs of a decode-context-parallel group, each running
+ * sparse_mla_decode (out_fp32 = 1) on its share of the top-k.
+ *
+ *   part_out   device fp32 [num_parts, num_q, num_heads, 512], 16-byte aligned:
+ *              each part's normalised output
+ *   part_lse   device fp32 [num_parts, num_q, num_heads]: each part's
+ *              natural-log LSE; -inf marks a part with no valid entry
+ *   num_parts  1..1024; num_heads 1..128; num_q >= 0 (0 is a no-op)
+ *   out        device [num_q, num_heads, 512]: bf16, or fp32 if out_fp32
+ *   lse        nullable device fp32 [num_q, num_heads]
+ * out = sum_p exp(lse_p - lse) * out_p and lse = ln sum_p exp(lse_p); a
+ * (token, head) whose parts are all empty gets out = 0 and lse = -inf.
+ * Equal to a single sparse_mla_decode over the union of the parts' entries
+ * up to fp32 rounding.
+ */
+int32_t sparse_mla_merge_states(const float* part_out, const float* part_lse, int32_t num_parts,
+                                int32_t num_q, int32_t num_heads, void* out, int32_t out_fp32,
+                                float* lse, void* stream);
+
+/*
  * The staged-dequant comparison path of section "Native NVFP4 sparse MLA
  * decode kernel": the post measures its fused kernel against a variant that
  * first dequantises the selected rows into an FP8 temporary buffer in device

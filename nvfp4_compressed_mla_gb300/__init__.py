@@ -28,7 +28,8 @@ __all__ = [
     "LATENT_DIM", "ROPE_DIM", "ROW_NVFP4_352", "ROW_FP8_576", "ROW_BYTES", "NativeError",
     "nvfp4_mla_row_bytes", "nvfp4_mla_status_string", "nvfp4_mla_append",
     "sparse_mla_decode_num_splits", "sparse_mla_decode_workspace_size", "sparse_mla_decode",
-    "nvfp4_mla_staged_rows_per_q", "nvfp4_mla_stage_fp8", "staged_fp8_tables", "library_path",
+    "sparse_mla_merge_states", "nvfp4_mla_staged_rows_per_q", "nvfp4_mla_stage_fp8",
+    "staged_fp8_tables", "library_path",
 ]
 
 
@@ -137,6 +138,23 @@ def sparse_mla_decode(q_latent: torch.Tensor, q_rope: torch.Tensor, q_seq: torch
     _check(st, "sparse_mla_decode")
     return out, lse
 
+
+def sparse_mla_merge_states(part_out: torch.Tensor, part_lse: torch.Tensor,
+                            out: Optional[torch.Tensor] = None, out_fp32: bool = False,
+                            lse: Optional[torch.Tensor] = None, stream=None):
+    """Merge P partial attention states (fp32 [P,num_q,H,512], [P,num_q,H]);
+    returns (out [num_q,H,512], lse [num_q,H])."""
+    P, num_q, H = part_out.shape[0], part_out.shape[1], part_out.shape[2]
+    dev = part_out.device
+    if out is None:
+        out = torch.empty((num_q, H, LATENT_DIM), device=dev,
+                          dtype=torch.float32 if out_fp32 else torch.bfloat16)
+    if lse is None:
+        lse = torch.empty((num_q, H), device=dev, dtype=torch.float32)
+    st = _lib().sparse_mla_merge_states(_ptr(part_out), _ptr(part_lse), P, num_q, H, _ptr(out),
+                                        1 if out_fp32 else 0, _ptr(lse), _stream(stream))
+    _check(st, "sparse_mla_merge_states")
+    return out, lse
 
 # ------------------------------------------------ staged-dequant comparison path
 def nvfp4_mla_staged_rows_per_q(topk: int, page_size: int) -> int:

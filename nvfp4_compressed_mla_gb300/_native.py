@@ -27,6 +27,7 @@ SIGNATURES = {
                                 F32, F32, F32, P, I32, P, P, SZ, I32, P, P]),
     "sparse_mla_decode_noalloc": (I32, [P, P, P, P, I32, I32, I32, P, I32, I32, P, I32, P, I64,
                                         I64, I32, F32, F32, F32, P, I32, P, I32, P, P]),
+    "sparse_mla_merge_states": (I32, [P, P, I32, I32, I32, P, I32, P, P]),
     "nvfp4_mla_staged_rows_per_q": (I64, [I32, I32]),
     "nvfp4_mla_stage_fp8": (I32, [P, P, I32, I32, P, I32, I32, P, I32, P, I64, I64, F32, P, P,
                                   P, P]),

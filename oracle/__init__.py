@@ -76,6 +76,8 @@ def _load():
             lib.orc_stage_fp8.argtypes = [P, P, i32, i32, P, i32, i32, P, i32, P, i64, i64, f32,
                                           i64, P, P]
             lib.orc_stage_fp8.restype = i64
+            lib.orc_merge_states.argtypes = [P, P, i32, i64, P, P]
+            lib.orc_merge_states.restype = None
             _lib = lib
     return _lib
 
@@ -213,3 +215,18 @@ def stage_fp8(q_seq, topk_idx, block_table, seq_lens, page_size: int, cache: np.
                                 bt.shape[1], _ptr(seq_lens), page_size, _ptr(cache), num_blocks,
                                 block_stride, latent_scale, R, _ptr(staged), _ptr(sidx))
     return staged, sidx, int(bad)
+
+
+# ------------------------------------------------------------ state merge
+def merge_states(part_out, part_lse):
+    """Merge P attention states: part_out [P, num_q, H, 512], part_lse [P, num_q, H]
+    (fp64) -> (out [num_q, H, 512], lse [num_q, H])."""
+    po = _c(part_out, np.float64)
+    pl = _c(part_lse, np.float64)
+    P = po.shape[0]
+    shape = pl.shape[1:]
+    states = int(np.prod(shape))
+    out = np.empty(shape + (LATENT_DIM,), np.float64)
+    lse = np.empty(shape, np.float64)
+    _load().orc_merge_states(_ptr(po), _ptr(pl), P, states, _ptr(out), _ptr(lse))
+    return out, lse

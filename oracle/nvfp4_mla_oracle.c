@@ -326,6 +326,36 @@ int64_t orc_stage_fp8(const int32_t* q_seq, const int32_t* topk_idx, int32_t num
   return bad;
 }
 
+/* Merge of attention states over disjoint parts of each query token's
+ * selection (section "Native NVFP4 sparse MLA decode kernel": a token's
+ * partial softmax results are merged; here parts from anywhere). Each part
+ * is a normalised output out_p [512] with its natural-log lse_p; with
+ * m = max_p lse_p: out = sum_p exp(lse_p - m) out_p / sum_p exp(lse_p - m),
+ * lse = m + ln sum_p exp(lse_p - m). All parts empty (-inf) -> 0, -inf.
+ * Layout: part_out [P][states][512], part_lse [P][states]. */
+void orc_merge_states(const double* part_out, const double* part_lse, int32_t num_parts,
+                      int64_t states, double* out, double* lse) {
+  for (int64_t i = 0; i < states; ++i) {
+    double m = -INFINITY;
+    for (int p = 0; p < num_parts; ++p)
+      if (part_lse[p * states + i] > m) m = part_lse[p * states + i];
+    double* o = out + i * ORC_LATENT;
+    for (int k = 0; k < ORC_LATENT; ++k) o[k] = 0.0;
+    if (m == -INFINITY) {
+      lse[i] = -INFINITY;
+      continue;
+    }
+    double tot = 0.0;
+    for (int p = 0; p < num_parts; ++p) {
+      double w = exp(part_lse[p * states + i] - m);
+      tot += w;
+      for (int k = 0; k < ORC_LATENT; ++k) o[k] += w * part_out[(p * states + i) * ORC_LATENT + k];
+    }
+    for (int k = 0; k < ORC_LATENT; ++k) o[k] /= tot;
+    lse[i] = m + log(tot);
+  }
+}
+
 int orc_max_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

@@ -458,3 +458,34 @@ def test_stage_fp8_matches_torch_reencoding_and_placement():
             assert np.array_equal(row_out[512:], row_in[288:])
             n_checked += 1
     assert n_checked == wl.num_q * wl.topk - 3
+
+
+# ------------------------------------------------------------ state merge
+def test_merge_of_disjoint_parts_equals_decode_of_their_union():
+    """Attention over a union of disjoint selections is the LSE-weighted merge of
+    the parts' normalised outputs (softmax over a union), to fp64 rounding; an
+    empty part contributes nothing; all parts empty gives 0 and -inf."""
+    wl = make_workload("tiny", num_seqs=2, seq_len=600, num_heads=4, topk=90, q_per_seq=2)
+    from workloads import all_tokens
+    seq, pos = all_tokens(wl)
+    lat, rope = make_rows(wl, int(seq.size))
+    stride = 64 * 352
+    pool = np.zeros(wl.num_blocks * stride, np.uint8)
+    assert oracle.append(lat, rope, seq, pos, wl.block_table, 64, pool, wl.num_blocks,
+                         stride) == 0
+    ql, qr = make_queries(wl)
+
+    def dec(idx):
+        o, l, _ = oracle.sparse_mla_decode(ql, qr, wl.q_seq, idx, wl.block_table, wl.seq_lens, 64,
+                                           pool, wl.num_blocks, stride, 0, wl.sm_scale)
+        return o, l
+    full, full_lse = dec(wl.topk_idx)
+    empty = np.full((wl.num_q, 5), -1, np.int32)
+    parts = [wl.topk_idx[:, :17], wl.topk_idx[:, 17:60], empty, wl.topk_idx[:, 60:]]
+    outs, lses = zip(*[dec(np.ascontiguousarray(p)) for p in parts])
+    out, lse = oracle.merge_states(np.stack(outs), np.stack(lses))
+    assert np.max(np.abs(out - full)) < 1e-12 * max(1.0, np.max(np.abs(full)))
+    assert np.max(np.abs(lse - full_lse)) < 1e-12 * max(1.0, np.max(np.abs(full_lse)))
+    o0, l0 = dec(empty)
+    out, lse = oracle.merge_states(np.stack([o0, o0]), np.stack([l0, l0]))
+    assert not out.any() and np.all(np.isneginf(lse))
