@@ -990,30 +990,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int u = 0; u < n_sub; ++u) {
           const int s2 = u & 1;
           const uint32_t k2 = u >> 1;
-          const int ha = 2 * u, hb = 2 * u + 1;
-          const int va = ha % L::kVSlots, vb = hb % L::kVSlots;
-          if (!wait_bar(bar(Ctl::kVtFull, va), (ha / L::kVSlots) & 1u, abort_addr)) break;
-          if (!wait_bar(bar(Ctl::kVtFull, vb), (hb / L::kVSlots) & 1u, abort_addr)) break;
+          // P (and any rescale of O) first; then each 32-row V slot is
+          // multiplied as soon as it is full and released by its own commit,
+          // so the dequant warps can refill it while the other slot's MMAs run
           if (!wait_bar<true>(bar(Ctl::kPFull, s2), k2 & 1u, abort_addr)) break;
           const uint4 fl = ld_shared_v4(ctl + Ctl::kAF + s2 * kAFBytes + 512);
           if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
             if (!wait_bar(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr)) break;
             ++n_corr;
           }
-          tc_fence_after();
           const uint32_t ptile = sbase + L::kP + s2 * L::kPTile;
+          bool run = true;
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t adesc = sw128_desc(ptile + kk * 32u);
-            const uint32_t vslot = sbase + (kk < 2 ? va : vb) * L::kVSlot + (kk & 1) * 2048u;
-#pragma unroll
-            for (int nh = 0; nh < 2; ++nh) {
-              const uint64_t bdesc = sw128_desc_mn(vslot + nh * 16384u);
-              mma_ss(tmem + 256u * nh, adesc, bdesc, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
+          for (int hh = 0; hh < 2; ++hh) {
+            const int hs = 2 * u + hh;
+            const int vs = hs % L::kVSlots;
+            if (!wait_bar(bar(Ctl::kVtFull, vs), (hs / L::kVSlots) & 1u, abort_addr)) {
+              run = false;
+              break;
             }
+            tc_fence_after();
+#pragma unroll
+            for (int k1 = 0; k1 < 2; ++k1) {
+              const int kk = 2 * hh + k1;
+              const uint64_t adesc = sw128_desc(ptile + kk * 32u);
+              const uint32_t vslot = sbase + vs * L::kVSlot + k1 * 2048u;
+#pragma unroll
+              for (int nh = 0; nh < 2; ++nh) {
+                const uint64_t bdesc = sw128_desc_mn(vslot + nh * 16384u);
+                mma_ss(tmem + 256u * nh, adesc, bdesc, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            mma_commit(bar(Ctl::kVtEmpty, vs));
+            last_bar = bar(Ctl::kVtEmpty, vs);  // tracks every MMA issued so far
+            last_parity = (hs / L::kVSlots) & 1u;
+            issued = true;
           }
-          mma_commit(bar(Ctl::kVtEmpty, va));
-          mma_commit(bar(Ctl::kVtEmpty, vb));
+          if (!run) break;
           mma_commit(bar(Ctl::kPvDone, s2));
           last_bar = bar(Ctl::kPvDone, s2);
           last_parity = k2 & 1u;
