@@ -309,30 +309,61 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride, fmt, splits,
             ws, world):
-    """Same step through the public Python API, inputs from pinned host memory each step."""
+    """Same step through the public Python API, inputs from pinned host memory each step.
+
+    Every step copies its inputs (queries, top-k, new tokens) host -> device and
+    its result (out, LSE) device -> host. The copies run on their own streams,
+    double-buffered, so step i + 1's inputs arrive and step i - 1's result
+    leaves while step i computes; events order each buffer's reuse.
+    """
     import torch
     layers = len(L)
+    keys = ("ql", "qr", "idx", "new_lat", "new_rope")
     host = []
     for d in L:
-        host.append({k: d[k].cpu().pin_memory() for k in ("ql", "qr", "idx", "new_lat",
-                                                           "new_rope")})
-    dbuf = {k: torch.empty_like(L[0][k]) for k in ("ql", "qr", "idx", "new_lat", "new_rope")}
-    out_h = torch.empty((wl.num_q, wl.num_heads, 512), dtype=torch.bfloat16).pin_memory()
-    lse_h = torch.empty((wl.num_q, wl.num_heads), dtype=torch.float32).pin_memory()
+        host.append({k: d[k].cpu().pin_memory() for k in keys})
+    dbuf = [{k: torch.empty_like(L[0][k]) for k in keys} for _ in range(2)]
+    dout = [(torch.empty((wl.num_q, wl.num_heads, 512), dtype=torch.bfloat16, device=dev),
+             torch.empty((wl.num_q, wl.num_heads), dtype=torch.float32, device=dev))
+            for _ in range(2)]
+    hout = [(torch.empty((wl.num_q, wl.num_heads, 512), dtype=torch.bfloat16).pin_memory(),
+             torch.empty((wl.num_q, wl.num_heads), dtype=torch.float32).pin_memory())
+            for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host[0].values())
-    d2h = out_h.numel() * 2 + lse_h.numel() * 4
+    d2h = hout[0][0].numel() * 2 + hout[0][1].numel() * 4
+    comp = torch.cuda.current_stream(dev)
+    cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    in_ready = [ev(), ev()]
+    used = [ev(), ev()]       # step's inputs and outputs are no longer needed by the compute
+    out_read = [ev(), ev()]   # step's result has reached the host
+    for b in range(2):        # every event starts out recorded
+        for e_ in (in_ready[b], used[b], out_read[b]):
+            e_.record(comp)
 
     def step(i):
+        b = i & 1
         h = host[i % layers]
-        for k in dbuf:
-            dbuf[k].copy_(h[k], non_blocking=True)
-        nm.nvfp4_mla_append(dbuf["new_lat"], dbuf["new_rope"], app_seq, app_pos, bt, 64,
-                            L[i % layers]["pool"], wl.num_blocks, stride, fmt)
-        o, l = nm.sparse_mla_decode(dbuf["ql"], dbuf["qr"], q_seq, dbuf["idx"], bt, seq_lens, 64,
-                                    L[i % layers]["pool"], wl.num_blocks, stride, fmt,
-                                    wl.sm_scale, workspace=ws, num_splits=splits)
-        out_h.copy_(o, non_blocking=True)
-        lse_h.copy_(l, non_blocking=True)
+        with torch.cuda.stream(cin):           # inputs of step i into buffer b
+            cin.wait_event(used[b])
+            for k in keys:
+                dbuf[b][k].copy_(h[k], non_blocking=True)
+            in_ready[b].record(cin)
+        comp.wait_event(in_ready[b])
+        comp.wait_event(out_read[b])           # buffer b's previous result has been read
+        d = dbuf[b]
+        nm.nvfp4_mla_append(d["new_lat"], d["new_rope"], app_seq, app_pos, bt, 64,
+                            L[i % layers]["pool"], wl.num_blocks, stride, fmt, stream=comp)
+        nm.sparse_mla_decode(d["ql"], d["qr"], q_seq, d["idx"], bt, seq_lens, 64,
+                             L[i % layers]["pool"], wl.num_blocks, stride, fmt, wl.sm_scale,
+                             out=dout[b][0], lse=dout[b][1], workspace=ws, num_splits=splits,
+                             stream=comp)
+        used[b].record(comp)
+        with torch.cuda.stream(cout):          # result of step i to the host
+            cout.wait_event(used[b])
+            hout[b][0].copy_(dout[b][0], non_blocking=True)
+            hout[b][1].copy_(dout[b][1], non_blocking=True)
+            out_read[b].record(cout)
 
     for i in range(5):
         step(i)
@@ -342,10 +373,12 @@ def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride,
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    s.record()
+    s.record(comp)
     for i in range(K):
         step(i)
-    e.record()
+    comp.wait_event(out_read[0])
+    comp.wait_event(out_read[1])
+    e.record(comp)
     torch.cuda.synchronize()
     ms = s.elapsed_time(e)
     if world > 1:
@@ -355,7 +388,8 @@ def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride,
     kv = wl.valid_slots() * ROW_BYTES[fmt]
     return {"value": round(kv * K * world / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "ms_per_step": round(ms / K, 5)}
+            "ms_per_step": round(ms / K, 5),
+            "copies": "host->device and device->host on their own streams, double-buffered"}
 
 
 # ------------------------------------------------------------ CPU oracle
