@@ -91,6 +91,22 @@ def algorithmic(wl, row_format):
     return {"kv_bytes": kv, "bytes": kv + q + out + idx, "flops": flops}
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time (every rank gets it); `device` holds the
+    reduction tensor (a CUDA device under nccl, None = CPU under gloo)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(kv_bytes_per_step: int, steps: int, world: int, ms: float) -> float:
+    """Compressed-KV GB/s of the whole job: every rank's steps over the slowest rank's time."""
+    return kv_bytes_per_step * steps * world / (ms * 1e-3) / 1e9
+
+
 # --------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -289,13 +305,9 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clocks = sampler.stop() if rank == 0 else None
-    total_ms = t_start.elapsed_time(t_end)
+    total_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
     append_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
     decode_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
 
     res = dict(total_ms=total_ms, append_ms=append_ms, decode_ms=decode_ms, layers=layers,
                splits=splits, clocks=clocks, wl=wl, alg=alg, fmt=fmt,
@@ -380,13 +392,9 @@ def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride,
     comp.wait_event(out_read[1])
     e.record(comp)
     torch.cuda.synchronize()
-    ms = s.elapsed_time(e)
-    if world > 1:
-        t = torch.tensor([ms], device=dev, dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(s.elapsed_time(e), world, dev)
     kv = wl.valid_slots() * ROW_BYTES[fmt]
-    return {"value": round(kv * K * world / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+    return {"value": round(whole_job_gbs(kv, K, world, ms), 3), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "ms_per_step": round(ms / K, 5),
             "copies": "host->device and device->host on their own streams, double-buffered"}
@@ -799,7 +807,7 @@ def main():
     wl, alg, fmt = res["wl"], res["alg"], res["fmt"]
     K = args.steps
     ms_step = res["total_ms"] / K
-    value = alg["kv_bytes"] * K * world / (res["total_ms"] * 1e-3) / 1e9
+    value = whole_job_gbs(alg["kv_bytes"], K, world, res["total_ms"])
     dec_s = res["decode_ms"] * 1e-3 / K
     achieved_tf = alg["flops"] / dec_s / 1e12
     achieved_gbs = alg["bytes"] / dec_s / 1e9
