@@ -10,8 +10,9 @@
 // bytes of bf16 input, 8 bytes of codes + 1 scale byte of output) and rope
 // values 2j, 2j+1. Every load is a coalesced 16-byte vector; the row is
 // written as 8-byte payload stores, 1-byte scales and 2-byte rope pairs
-// that together cover whole 32-byte sectors. HBM-bound: 1152 bytes read and
-// 352 written per token.
+// that together cover whole 32-byte sectors. The token's values are loaded
+// before its slot is resolved, so those loads overlap the index and
+// block-table loads. HBM-bound: 1152 bytes read and 352 written per token.
 #include <math.h>
 
 #include "common.cuh"
@@ -20,6 +21,13 @@ namespace nvfp4_mla {
 namespace {
 
 constexpr int kAppendWarps = 8;
+
+// x / s rounded to fp32. For a power-of-two s the product with its exact
+// reciprocal is the same correctly rounded value, without the division's
+// instruction sequence.
+__device__ __forceinline__ float div_scale(float x, float s, float inv_pow2) {
+  return inv_pow2 != 0.f ? x * inv_pow2 : __fdiv_rn(x, s);
+}
 
 // E2M1 code of x under scale S > 0: nearest grid value of x/S, ties to the
 // even code, saturating at 6, sign from x. Decided by comparing |x| with
@@ -39,11 +47,15 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
                   int32_t n_tok, const int32_t* __restrict__ block_table, int32_t num_seqs,
                   int32_t max_blocks, int32_t page_size, uint8_t* __restrict__ cache,
                   int64_t num_blocks, int64_t block_stride, float latent_scale, float rope_scale,
-                  int32_t* __restrict__ invalid_count) {
+                  float inv_latent_pow2, float inv_rope_pow2, int32_t* __restrict__ invalid_count) {
   constexpr int kRowBytes = kFmt == NVFP4_MLA_ROW_NVFP4_352 ? kNvfp4Row : kFp8Row;
   const int lane = threadIdx.x & 31;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * kAppendWarps + (threadIdx.x >> 5);
   if (t >= n_tok) return;
+  const uint8_t* src = latent + t * (kLatent * 2) + lane * (kGroup * 2);
+  const uint4 a = ld_nc_v4(src);
+  const uint4 b = ld_nc_v4(src + 16);
+  const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + t * (kRope * 2)) + lane);
   const int64_t off = resolve_row(__ldg(seq_ids + t), __ldg(positions + t), -1, block_table,
                                   num_seqs, max_blocks, page_size, num_blocks, block_stride,
                                   kRowBytes);
@@ -53,9 +65,6 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
   }
   uint8_t* row = cache + off;
 
-  const uint8_t* src = latent + t * (kLatent * 2) + lane * (kGroup * 2);
-  const uint4 a = ld_nc_v4(src);
-  const uint4 b = ld_nc_v4(src + 16);
   const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
   float x[kGroup];
 #pragma unroll
@@ -87,18 +96,17 @@ __global__ void __launch_bounds__(kAppendWarps * 32)
     uint32_t o[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t p0 = cvt_e4m3x2(__fdiv_rn(x[4 * i + 1], latent_scale),
-                                     __fdiv_rn(x[4 * i], latent_scale));
-      const uint32_t p1 = cvt_e4m3x2(__fdiv_rn(x[4 * i + 3], latent_scale),
-                                     __fdiv_rn(x[4 * i + 2], latent_scale));
+      const uint32_t p0 = cvt_e4m3x2(div_scale(x[4 * i + 1], latent_scale, inv_latent_pow2),
+                                     div_scale(x[4 * i], latent_scale, inv_latent_pow2));
+      const uint32_t p1 = cvt_e4m3x2(div_scale(x[4 * i + 3], latent_scale, inv_latent_pow2),
+                                     div_scale(x[4 * i + 2], latent_scale, inv_latent_pow2));
       o[i] = p0 | (p1 << 16);
     }
     *reinterpret_cast<uint4*>(row + lane * 16) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 
-  const uint32_t rw = __ldg(reinterpret_cast<const uint32_t*>(rope + t * (kRope * 2)) + lane);
-  const uint32_t r8 = cvt_e4m3x2(__fdiv_rn(bf16_hi(rw), rope_scale),
-                                 __fdiv_rn(bf16_lo(rw), rope_scale));
+  const uint32_t r8 = cvt_e4m3x2(div_scale(bf16_hi(rw), rope_scale, inv_rope_pow2),
+                                 div_scale(bf16_lo(rw), rope_scale, inv_rope_pow2));
   constexpr int kRopeAt = kFmt == NVFP4_MLA_ROW_NVFP4_352 ? kRopeOff : kLatent;
   *reinterpret_cast<uint16_t*>(row + kRopeAt + lane * 2) = static_cast<uint16_t>(r8);
 }
@@ -134,6 +142,12 @@ extern "C" int32_t nvfp4_mla_append(const void* latent, const void* rope, const 
   if (int32_t st = current_device_checked(&dev, &sms)) return st;
 
   const dim3 grid((n_tok + kAppendWarps - 1) / kAppendWarps);
+  auto inv_pow2 = [](float v) {  // 1/v when v is a power of two (exact), else 0
+    int e = 0;
+    return frexpf(v, &e) == 0.5f ? 1.0f / v : 0.0f;
+  };
+  const float inv_l = row_format == NVFP4_MLA_ROW_FP8_576 ? inv_pow2(latent_scale) : 0.0f;
+  const float inv_r = inv_pow2(rope_scale);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const auto* l = static_cast<const uint8_t*>(latent);
   const auto* r = static_cast<const uint8_t*>(rope);
@@ -141,10 +155,10 @@ extern "C" int32_t nvfp4_mla_append(const void* latent, const void* rope, const 
   if (row_format == NVFP4_MLA_ROW_NVFP4_352)
     append_kernel<NVFP4_MLA_ROW_NVFP4_352><<<grid, kAppendWarps * 32, 0, s>>>(
         l, r, seq_ids, positions, n_tok, block_table, num_seqs, max_blocks_per_seq, page_size, c,
-        num_blocks, block_stride_bytes, latent_scale, rope_scale, invalid_count);
+        num_blocks, block_stride_bytes, latent_scale, rope_scale, inv_l, inv_r, invalid_count);
   else
     append_kernel<NVFP4_MLA_ROW_FP8_576><<<grid, kAppendWarps * 32, 0, s>>>(
         l, r, seq_ids, positions, n_tok, block_table, num_seqs, max_blocks_per_seq, page_size, c,
-        num_blocks, block_stride_bytes, latent_scale, rope_scale, invalid_count);
+        num_blocks, block_stride_bytes, latent_scale, rope_scale, inv_l, inv_r, invalid_count);
   return launch_status();
 }
