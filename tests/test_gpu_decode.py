@@ -7,6 +7,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from tests.gpu_cases import (TOL_REL_L2, assert_parity, build_case, dev_tensor, gpu_decode,
                              oracle_decode, rel_l2)
 from workloads import make_workload
@@ -130,3 +131,23 @@ def test_full_size_config(name):
 @pytest.mark.parametrize("row_format", [0, 1])
 def test_full_size_append_dense(row_format):
     _full("append_dense", row_format, sample=2)
+
+
+# -------------------------------------------------- the largest top-k the ABI accepts
+@pytest.mark.parametrize("splits", [0, 1])
+def test_maximum_topk(splits):
+    """topk = 65536 (512 tiles; automatic splits and one cluster walking all of them),
+    128 heads, a -1 tail; the oracle checks a few heads (its cost grows with H)."""
+    wl = make_workload("tiny", num_seqs=1, seq_len=70000, num_heads=128, topk=65536,
+                       q_per_seq=1)
+    case = build_case(wl, "referenced")
+    idx = wl.topk_idx.copy()
+    idx[:, -1000:] = -1
+    out, lse = gpu_decode(case, num_splits=splits, idx=dev_tensor(idx))
+    heads = np.array([0, 37, 127])
+    ref, ref_lse, bad = oracle.sparse_mla_decode(
+        case.ql[:, heads], case.qr[:, heads], wl.q_seq, idx, wl.block_table, wl.seq_lens,
+        wl.page_size, case.host_pool, wl.num_blocks, case.stride, 0, wl.sm_scale)
+    assert bad == 0
+    assert_parity(out[:, heads], lse[:, heads], ref, ref_lse)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
