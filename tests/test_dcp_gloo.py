@@ -67,6 +67,10 @@ def test_two_ranks():
     _run(2)
 
 
+def test_three_ranks_ragged_shards():
+    _run(3)  # 150 columns over 3 ranks
+
+
 def test_shard_bounds_cover_the_selection():
     from nvfp4_compressed_mla_gb300 import dcp
     for topk in (1, 5, 128, 2048, 2049):
