@@ -154,3 +154,76 @@ def test_valid_arguments_without_gpu_report_device(lib):
         pytest.skip("a GPU is present")
     assert _append(lib) in (4, 9)
     assert _decode(lib) in (4, 9)
+
+
+# ------------------------------------------ staged comparison path and state merge
+def _stage(lib, **kw):
+    a = dict(q_seq=FAKE, idx=FAKE, num_q=2, topk=100, bt=FAKE, num_seqs=1, max_blocks=4,
+             seq_lens=FAKE, page_size=64, cache=FAKE, num_blocks=4, block_stride=64 * 352,
+             latent_scale=1.0, staged=FAKE, staged_idx=FAKE, invalid=None, stream=None)
+    a.update(kw)
+    return lib.nvfp4_mla_stage_fp8(a["q_seq"], a["idx"], a["num_q"], a["topk"], a["bt"],
+                                   a["num_seqs"], a["max_blocks"], a["seq_lens"], a["page_size"],
+                                   a["cache"], a["num_blocks"], a["block_stride"],
+                                   a["latent_scale"], a["staged"], a["staged_idx"], a["invalid"],
+                                   a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(topk=0), ERR_SHAPE),
+    (dict(topk=65537), ERR_SHAPE),
+    (dict(page_size=0), ERR_SHAPE),
+    (dict(num_q=-1), ERR_SHAPE),
+    (dict(staged=None), ERR_NULL),
+    (dict(staged_idx=None), ERR_NULL),
+    (dict(cache=None), ERR_NULL),
+    (dict(block_stride=64 * 352 - 16), ERR_SHAPE),
+    (dict(block_stride=64 * 352 + 8), ERR_ALIGN),
+    (dict(staged=FAKE + 4), ERR_ALIGN),
+    (dict(latent_scale=-1.0), ERR_VALUE),
+    (dict(latent_scale=float("nan")), ERR_VALUE),
+])
+def test_stage_rejects_bad_arguments(lib, kw, status):
+    assert _stage(lib, **kw) == status
+
+
+def test_stage_zero_queries_and_rows_per_query(lib):
+    assert _stage(lib, num_q=0, staged=None) == 0
+    assert lib.nvfp4_mla_staged_rows_per_q(100, 64) == 128
+    assert lib.nvfp4_mla_staged_rows_per_q(128, 64) == 128
+    assert lib.nvfp4_mla_staged_rows_per_q(1, 16) == 16
+    assert lib.nvfp4_mla_staged_rows_per_q(0, 64) == 0
+    assert lib.nvfp4_mla_staged_rows_per_q(10, 0) == 0
+
+
+def _merge(lib, **kw):
+    a = dict(part_out=FAKE, part_lse=FAKE, parts=2, num_q=3, heads=16, out=FAKE, out_fp32=0,
+             lse=None, stream=None)
+    a.update(kw)
+    return lib.sparse_mla_merge_states(a["part_out"], a["part_lse"], a["parts"], a["num_q"],
+                                       a["heads"], a["out"], a["out_fp32"], a["lse"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(parts=0), ERR_SHAPE),
+    (dict(parts=1025), ERR_SHAPE),
+    (dict(heads=0), ERR_SHAPE),
+    (dict(heads=129), ERR_SHAPE),
+    (dict(num_q=-2), ERR_SHAPE),
+    (dict(part_out=None), ERR_NULL),
+    (dict(part_lse=None), ERR_NULL),
+    (dict(out=None), ERR_NULL),
+    (dict(part_out=FAKE + 4), ERR_ALIGN),
+    (dict(out=FAKE + 8), ERR_ALIGN),
+])
+def test_merge_rejects_bad_arguments(lib, kw, status):
+    assert _merge(lib, **kw) == status
+
+
+def test_new_entry_points_without_gpu_report_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert _stage(lib) in (4, 9)
+    assert _merge(lib) in (4, 9)
+    assert _merge(lib, num_q=0) == 0
