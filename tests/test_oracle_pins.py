@@ -291,6 +291,87 @@ def test_append_skips_and_counts_unresolvable_tokens():
     assert cache.reshape(-1, 352).any(1).sum() == 1
 
 
+# ------------------------------------------- row decode, independent of the oracle
+def _grid_from_golden() -> np.ndarray:
+    """E2M1 value of each of the 16 codes, from the definition in tests/golden."""
+    g = np.zeros(16, np.float64)
+    for code, val in read_golden("e2m1_grid.txt"):
+        g[int(code)] = float(val)
+    return g
+
+
+def indep_dequant(rows: np.ndarray, rope_scale: float = 1.0):
+    """Decode 352-byte rows without the oracle: nibble split, the golden E2M1
+    grid, torch's float8_e4m3fn view of the scale and rope bytes (row layout:
+    codes at 0..255, scales at 256..287, rope at 288..351)."""
+    rows = np.ascontiguousarray(rows, np.uint8).reshape(-1, 352)
+    grid = _grid_from_golden()
+    codes = np.empty((rows.shape[0], 512), np.uint8)
+    codes[:, 0::2] = rows[:, :256] & 15
+    codes[:, 1::2] = rows[:, :256] >> 4
+
+    def e4m3_view(b):
+        return torch.from_numpy(np.ascontiguousarray(b)).view(torch.float8_e4m3fn).double().numpy()
+
+    scales = e4m3_view(rows[:, 256:288])
+    lat = grid[codes] * np.repeat(scales, 16, axis=1)
+    rope = e4m3_view(rows[:, 288:352]) * float(np.float32(rope_scale))
+    return lat, rope
+
+
+@pytest.mark.parametrize("rs", [0.37, 3.0, 1.0])
+def test_nvfp4_rope_dequant_is_e4m3_view_times_rope_scale(rs):
+    """The rope part of an NVFP4 row is kept FP8 (the Prime Inference post,
+    section "Making room for low-latency decode"), read back as E4M3 times the
+    per-tensor rope scale."""
+    rng = np.random.default_rng(11)
+    # every finite E4M3 code (both signs) appears in the rope bytes of some row
+    finite = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], np.uint8)
+    n = (finite.size + 63) // 64
+    rows = rng.integers(0, 256, (n, 352), dtype=np.uint8)
+    rows[:, 256:288] &= 0x7E  # positive, finite scale bytes
+    rope_bytes = np.resize(finite, n * 64).reshape(n, 64)
+    rows[:, 288:352] = rope_bytes
+    lat, rope = oracle.dequant_rows(rows, 0, 1.0, rs)
+    want_lat, want_rope = indep_dequant(rows, rs)
+    assert np.array_equal(rope, want_rope)
+    assert np.array_equal(lat, want_lat)
+
+
+def test_nvfp4_dense_attention_with_rope_scale_matches_torch():
+    """Decode over NVFP4 rows written with rope_scale != 1 equals torch's dense
+    fp64 softmax(QK^T)V over rows decoded without the oracle."""
+    rs = 1.5
+    wl = make_workload("tiny", seq_len=160, num_heads=4)
+    lat_bf, rope_bf = make_rows(wl, 160)
+    cache = np.zeros(wl.num_blocks * 64 * 352, np.uint8)
+    oracle.append(lat_bf, rope_bf, np.zeros(160, np.int32), np.arange(160, dtype=np.int32),
+                  wl.block_table, 64, cache, wl.num_blocks, 64 * 352, 0, 1.0, rs)
+    ql, qr = make_queries(wl)
+    idx = np.arange(160, dtype=np.int32)[None, :]
+    out, lse, bad = oracle.sparse_mla_decode(ql, qr, wl.q_seq, idx, wl.block_table, wl.seq_lens,
+                                             64, cache, wl.num_blocks, 64 * 352, 0, wl.sm_scale,
+                                             1.0, rs)
+    assert bad == 0
+    rows = np.stack([cache.reshape(-1, 352)[wl.block_table[0, p // 64] * 64 + p % 64]
+                     for p in range(160)])
+    L, R = indep_dequant(rows, rs)
+    Q = torch.from_numpy(f32_from_bf16(ql[0]).astype(np.float64))
+    QR = torch.from_numpy(f32_from_bf16(qr[0]).astype(np.float64))
+    s = wl.sm_scale * (Q @ torch.from_numpy(L).T + QR @ torch.from_numpy(R).T)
+    want = torch.softmax(s, -1) @ torch.from_numpy(L)
+    assert np.allclose(out[0], want.numpy(), rtol=1e-12, atol=1e-13)
+    assert np.allclose(lse[0], torch.logsumexp(s, -1).numpy(), rtol=0, atol=1e-12)
+    # one selected row: out is exactly that row's latent, LSE its score
+    one = np.full((1, 8), -1, np.int32)
+    one[0, 3] = 97
+    o1, l1, _ = oracle.sparse_mla_decode(ql, qr, wl.q_seq, one, wl.block_table, wl.seq_lens, 64,
+                                         cache, wl.num_blocks, 64 * 352, 0, wl.sm_scale, 1.0, rs)
+    assert np.array_equal(o1[0], np.repeat(L[97][None], 4, 0))
+    z = wl.sm_scale * (Q.numpy() @ L[97] + QR.numpy() @ R[97])
+    assert np.allclose(l1[0], z, rtol=0, atol=1e-12)
+
+
 # ------------------------------------------------------------- attention
 def _setup(name="tiny", seed=None, **kw):
     wl = make_workload(name, seed=seed, **kw)
