@@ -233,7 +233,13 @@ extern "C" int32_t sparse_mla_decode_noalloc(
   void* scratch = nullptr;
   if (num_q > 0 && shape_ok(num_q, num_heads, topk) && num_splits >= 0 && num_splits <= 64) {
     const size_t need = sparse_mla_decode_workspace_size(num_q, num_heads, topk, num_splits);
-    if (need == SIZE_MAX) return NVFP4_MLA_ERR_DEVICE;
+    // The shape was validated just above, so SIZE_MAX here can only come from
+    // the device query inside the split planning (no device, or not sm_103).
+    if (need == SIZE_MAX) {
+      int dev = 0, sms = 0;
+      const int32_t st = current_device_checked(&dev, &sms);
+      return st != NVFP4_MLA_OK ? st : NVFP4_MLA_ERR_DEVICE;
+    }
     if (need > kNoAllocScratch) return NVFP4_MLA_ERR_WORKSPACE;
     if (need > 0) {
       if (int32_t st = noalloc_scratch(&scratch)) return st;

@@ -793,6 +793,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t mask = *reinterpret_cast<volatile uint64_t*>(
           smem + L::kCtl + Ctl::kMaskRing + 8 * (ur & 31));
       const bool ok = (mask >> (row & 63)) & 1ull;
+      // Reads below stay within bytes [0, row bytes) of the row slot (NVFP4:
+      // codes < 256, scales < 288, rope < 352; FP8: < 576), so the 16 pad bytes
+      // that the per-row bulk copies leave unwritten are never read.
       const uint32_t src = raw_row(sr, row & 63);
       // one chunk: wait for its ring slot, store 32 FP16 values, signal the MMA
       auto put_chunk = [&](int kb, const uint32_t (&h)[16]) -> bool {

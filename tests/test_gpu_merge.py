@@ -7,7 +7,8 @@ import pytest
 import torch
 
 import oracle
-from tests.gpu_cases import assert_parity, build_case, dev_tensor, oracle_decode, rel_l2
+from tests.gpu_cases import (TOL_REL_L2, assert_parity, build_case, dev_tensor, oracle_decode,
+                             rel_l2)
 from workloads import make_workload
 
 pytestmark = pytest.mark.gpu
@@ -27,7 +28,9 @@ def test_merge_matches_oracle(parts, out_fp32):
     torch.cuda.synchronize()
     ref, ref_lse = oracle.merge_states(po.astype(np.float64), pl.astype(np.float64))
     got = out.double().cpu().numpy()
-    tol = 1e-5 if out_fp32 else 8e-3
+    # bf16 output: round-to-nearest to 8 significant bits alone gives about
+    # 2^-8 / sqrt(7) = 1.5e-3 relative L2 on values spread over a binade
+    tol = 1e-5 if out_fp32 else TOL_REL_L2
     assert np.all(rel_l2(got, ref) <= tol)
     gl = lse.double().cpu().numpy()
     assert np.array_equal(np.isneginf(gl), np.isneginf(ref_lse))
