@@ -178,6 +178,21 @@ int32_t sparse_mla_decode(const void* q_latent, const void* q_rope, const int32_
                           int32_t* invalid_count, void* stream);
 
 /*
+ * Bound of the decode kernel's internal waits (for gathered rows, for a
+ * pipeline slot, for the partner SM of its cluster), in SM clock cycles.
+ * A wait that runs out makes its (query token, split) unit give up: the
+ * unit drains the copies and tensor-core work it has in flight, frees its
+ * tensor memory and writes NaN to its outputs and LSE (or workspace
+ * partials), so a stalled launch ends with a visible result instead of
+ * holding its SMs. 0 restores the default of 2^31 cycles (about a second).
+ * Process-wide; applies to decode launches enqueued after the call. A bound
+ * shorter than a healthy launch's waits makes healthy launches fail, which
+ * is how the failure path is tested. Returns NVFP4_MLA_ERR_VALUE if
+ * cycles < 0. This is this library's choice; the post has no counterpart.
+ */
+int32_t nvfp4_mla_set_wait_limit(int64_t cycles);
+
+/*
  * sparse_mla_decode without a caller-provided workspace. The paper has no
  * counterpart to this entry point; it exists for callers that cannot
  * allocate device memory themselves -- for example a plugin whose host

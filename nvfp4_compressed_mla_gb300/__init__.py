@@ -28,6 +28,7 @@ __all__ = [
     "LATENT_DIM", "ROPE_DIM", "ROW_NVFP4_352", "ROW_FP8_576", "ROW_BYTES", "NativeError",
     "nvfp4_mla_row_bytes", "nvfp4_mla_status_string", "nvfp4_mla_append",
     "sparse_mla_decode_num_splits", "sparse_mla_decode_workspace_size", "sparse_mla_decode",
+    "nvfp4_mla_set_wait_limit",
     "sparse_mla_merge_states", "nvfp4_mla_staged_rows_per_q", "nvfp4_mla_stage_fp8",
     "staged_fp8_tables", "library_path",
 ]
@@ -94,6 +95,11 @@ def nvfp4_mla_append(latent: torch.Tensor, rope: torch.Tensor, seq_ids: torch.Te
 
 def sparse_mla_decode_num_splits(num_q: int, num_heads: int, topk: int) -> int:
     return int(_lib().sparse_mla_decode_num_splits(num_q, num_heads, topk))
+
+
+def nvfp4_mla_set_wait_limit(cycles: int) -> None:
+    """Bound (SM clock cycles) of the decode kernel's internal waits; 0 = default."""
+    _check(_lib().nvfp4_mla_set_wait_limit(int(cycles)), "nvfp4_mla_set_wait_limit")
 
 
 def sparse_mla_decode_workspace_size(num_q: int, num_heads: int, topk: int,

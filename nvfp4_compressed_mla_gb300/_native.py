@@ -22,6 +22,7 @@ SIGNATURES = {
     "nvfp4_mla_append": (I32, [P, P, P, P, I32, P, I32, I32, I32, P, I64, I64, I32, F32, F32,
                                P, P]),
     "sparse_mla_decode_num_splits": (I32, [I32, I32, I32]),
+    "nvfp4_mla_set_wait_limit": (I32, [I64]),
     "sparse_mla_decode_workspace_size": (SZ, [I32, I32, I32, I32]),
     "sparse_mla_decode": (I32, [P, P, P, P, I32, I32, I32, P, I32, I32, P, I32, P, I64, I64, I32,
                                 F32, F32, F32, P, I32, P, P, SZ, I32, P, P]),

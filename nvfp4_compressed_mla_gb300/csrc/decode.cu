@@ -29,11 +29,18 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p) {
   const int S = p.num_splits;
   const float* wl = p.ws + static_cast<int64_t>(p.num_q) * S * p.num_heads * kLatent;
   float m = -INFINITY;
-  for (int s = 0; s < S; ++s)
-    m = fmaxf(m, wl[(static_cast<int64_t>(t) * S + s) * p.num_heads + h]);
+  bool failed = false;  // a split that gave up (its partial LSE is NaN) fails the token
+  for (int s = 0; s < S; ++s) {
+    const float ls = wl[(static_cast<int64_t>(t) * S + s) * p.num_heads + h];
+    failed |= isnan(ls);
+    m = fmaxf(m, ls);
+  }
   float acc[4] = {0.f, 0.f, 0.f, 0.f};
   float tot = 0.f;
-  if (m != -INFINITY) {
+  if (failed) {
+    acc[0] = acc[1] = acc[2] = acc[3] = NAN;
+    tot = NAN;
+  } else if (m != -INFINITY) {
     for (int s = 0; s < S; ++s) {
       const int64_t part = (static_cast<int64_t>(t) * S + s) * p.num_heads + h;
       const float ls = wl[part];
@@ -48,7 +55,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p) {
       }
     }
   }
-  const float sc = tot > 0.f ? p.out_mult / tot : 0.f;
+  const float sc = failed ? 1.f : (tot > 0.f ? p.out_mult / tot : 0.f);
   const int64_t qh = static_cast<int64_t>(t) * p.num_heads + h;
   const int d = threadIdx.x * 4;
   if (p.out_fp32) {
@@ -58,7 +65,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p) {
     *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + qh * kLatent + d) =
         make_uint2(pack_bf16x2(acc[0] * sc, acc[1] * sc), pack_bf16x2(acc[2] * sc, acc[3] * sc));
   }
-  if (threadIdx.x == 0 && p.lse != nullptr) p.lse[qh] = tot > 0.f ? m + lg2(tot) * kLn2 : -INFINITY;
+  if (threadIdx.x == 0 && p.lse != nullptr)
+    p.lse[qh] = failed ? NAN : (tot > 0.f ? m + lg2(tot) * kLn2 : -INFINITY);
 }
 
 // Splits per query token: enough (token, split) clusters to fill the GPU
@@ -90,10 +98,23 @@ size_t workspace_bytes_for(int num_q, int num_heads, int splits) {
   return static_cast<size_t>(num_q) * splits * num_heads * (kLatent + 1) * sizeof(float);
 }
 
+constexpr long long kDefaultWaitCycles = 1ll << 31;  // about a second at GB300 clocks
+std::atomic<long long> g_wait_cycles{kDefaultWaitCycles};
+
 }  // namespace
+
+long long decode_wait_cycles() { return g_wait_cycles.load(std::memory_order_relaxed); }
+
 }  // namespace nvfp4_mla
 
 using namespace nvfp4_mla;
+
+extern "C" int32_t nvfp4_mla_set_wait_limit(int64_t cycles) {
+  if (cycles < 0) return NVFP4_MLA_ERR_VALUE;
+  g_wait_cycles.store(cycles == 0 ? kDefaultWaitCycles : static_cast<long long>(cycles),
+                      std::memory_order_relaxed);
+  return NVFP4_MLA_OK;
+}
 
 extern "C" int32_t sparse_mla_decode_num_splits(int32_t num_q, int32_t num_heads, int32_t topk) {
   if (!shape_ok(num_q, num_heads, topk)) return 0;
@@ -169,6 +190,7 @@ extern "C" int32_t sparse_mla_decode(
   p.out_fp32 = out_fp32 ? 1 : 0;
   p.lse = lse;
   p.invalid_count = invalid_count;
+  p.wait_cycles = decode_wait_cycles();
   plan_splits(topk, num_splits ? num_splits : auto_splits(num_q, num_heads, topk, sms),
               &p.num_splits, &p.tiles_per_split, &p.num_tiles);
   const size_t need = workspace_bytes_for(num_q, num_heads, p.num_splits);

@@ -32,7 +32,12 @@ struct DecodeParams {
   int32_t num_splits, tiles_per_split, num_tiles;
   int32_t* invalid_count;
   int32_t use_tma;    // rows gathered with tile::gather4 tensor copies (else one bulk copy per row)
+  long long wait_cycles;  // bound of every wait inside the kernel (clock cycles)
 };
+
+// Bound of the decode kernel's waits: the default, or the process-wide
+// override set through nvfp4_mla_set_wait_limit.
+long long decode_wait_cycles();
 
 // Enqueue the tensor-core decode kernel (one 2-CTA cluster per (token, split)).
 int32_t launch_decode_tc(const DecodeParams& p, int row_format, cudaStream_t stream);

@@ -54,6 +54,12 @@ def test_row_bytes_and_status_strings(lib):
     assert lib.nvfp4_mla_status_string(99).decode() == "unknown status"
 
 
+def test_wait_limit_setting(lib):
+    assert lib.nvfp4_mla_set_wait_limit(-1) == 8  # NVFP4_MLA_ERR_VALUE
+    assert lib.nvfp4_mla_set_wait_limit(5000) == 0
+    assert lib.nvfp4_mla_set_wait_limit(0) == 0   # back to the default
+
+
 def test_workspace_size_host_logic(lib):
     big = (1 << 64) - 1
     # invalid shapes
