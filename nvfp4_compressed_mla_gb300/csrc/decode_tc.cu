@@ -31,12 +31,13 @@
 //     uses), rescale O and l when the score CTA raised its reference maximum,
 //     hand P buffers back, and write the normalised output at the end.
 //
-// Both CTAs gather their own copy of the rows: a producer warp resolves
-// top-k slots through the block table (-1 and unresolvable slots issue no
-// load), four 32-slot stages at a time, and publishes per stage the rows'
-// byte offsets and a live-row mask. A gather warp copies the live rows with
-// tile::gather4 tensor copies (four rows per copy; one bulk copy per row when
-// the page stride is not a whole number of rows). Every wait is bounded; a
+// Both CTAs gather their own copy of the rows: two gather warps take
+// alternate 32-slot stages, resolve the stage's top-k slots through the block
+// table (-1 and unresolvable slots issue no load; the index and block-table
+// loads run two of the warp's stages ahead), publish the stage's live-row
+// mask and copy the live rows with tile::gather4 tensor copies (four rows per
+// copy; one bulk copy per row when the page stride is not a whole number of
+// rows). Every wait is bounded; a
 // wait that runs out sets an abort flag, the roles unwind, copies and MMAs in
 // flight are drained, tensor memory is freed, and the unit's outputs are NaN.
 #include <cuda.h>
@@ -54,7 +55,7 @@ constexpr int kSub = 32;                     // rows per gather stage / P piece 
 constexpr int kPiecesPerTile = kTile / kSub;  // 4
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kProducerWarp = 4, kMmaWarp = 5, kGatherWarp = 6;
+constexpr int kMmaWarp = 5, kGatherWarp = 6;  // gather warps 6 and 7; warp 4 has no role
 constexpr int kDequantWarp0 = 8;             // warps 8..15; warp w runs on sub-partition w % 4
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunksPerTile = 9;            // 8 latent chunks + the rope chunk
@@ -68,7 +69,12 @@ constexpr int kVSlots = 3;                   // output CTA: V slots of 32 rows
 // cannot tell those phases apart). With four pairs every waiter is at most
 // one phase ahead.
 constexpr int kRawBars = 4;
-constexpr float kTau = 8.0f;                 // lazy rescale threshold (log2 units)
+// Lazy rescale threshold (log2 units): a head's reference maximum moves only
+// when a score exceeds it by more than kTau, so P = 2^(s c - m_ref) <= 2^15,
+// which FP16 holds (largest finite value 65504); l <= 2^15 x top-k stays far
+// inside FP32. A P value is never below its exact-maximum counterpart, so the
+// headroom costs no precision.
+constexpr float kTau = 15.0f;
 constexpr long long kDrainCycles = 1ll << 31;
 // tcgen05 instruction descriptors (kind::f16, FP16 A/B, FP32 D):
 //   bit 4 D = f32, bit 15 A MN-major, bit 16 B MN-major, N >> 3 at 17, M >> 4 at 24
@@ -107,16 +113,12 @@ struct TcLayout {
   static constexpr int kStageO = (kSub / 4) * kGroupO;
   static constexpr int kStagesS = kNv ? 4 : 2;
   static constexpr int kStagesO = kNv ? 4 : 3;
-  static constexpr int kOffsSlots = 8;                      // resolved stages in flight
-  static constexpr int kOffsSlot = kSub * 8 + 8;            // 32 byte offsets + live mask
-  static constexpr int kOffsBytes = kOffsSlots * kOffsSlot;
   // score CTA
   static constexpr int kQTile = 16384;                      // 128 heads x 64 dims (SW128)
   static constexpr int kQ = 0;                              // 9 tiles: 8 latent + rope
   static constexpr int kRawS = kQ + kChunksPerTile * kQTile;
   static constexpr int kStg = kRawS + kStagesS * kStageS;   // 4 P^T staging slots
-  static constexpr int kOffsS = kStg + kPiecesPerTile * kPiece;
-  static constexpr int kNegM = kOffsS + kOffsBytes;         // -(reference maximum) per head
+  static constexpr int kNegM = kStg + kPiecesPerTile * kPiece;  // -(reference maximum) per head
   static constexpr int kAlpha = kNegM + 512;                // rescale factor per head
   static constexpr int kFlags = kAlpha + 512;               // per softmax warp: "rescaled"
   static constexpr int kAFS = kFlags + 16;                  // factors + flags of slot 0, flags 1-3
@@ -125,8 +127,7 @@ struct TcLayout {
   static constexpr int kVSlot = 32 * 1024;                  // 32 rows x 512 dims FP16 (MN-major)
   static constexpr int kP = kVSlots * kVSlot;               // kPBufs P^T pieces
   static constexpr int kRawO = kP + kPBufs * kPiece;
-  static constexpr int kOffsO = kRawO + kStagesO * kStageO;
-  static constexpr int kAFO = kOffsO + kOffsBytes;          // factors + flags per P buffer
+  static constexpr int kAFO = kRawO + kStagesO * kStageO;  // factors + flags per P buffer
   static constexpr int kFinO = kAFO + kPBufs * kAFBytes;    // final reference maximum per head
   static constexpr int kEndO = kFinO + 512;
   static constexpr int kCtl = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
@@ -142,8 +143,7 @@ struct TcLayout {
 
 // Control block (barriers and a few words): same offset in both CTAs of the cluster.
 struct Ctl {
-  static constexpr int kRawFull = 0, kRawEmpty = 32, kOffsFull = 64, kOffsEmpty = 128,
-                       kChunkFull = 192, kChunkEmpty = 264, kSFull = 336, kSEmpty = 352,
+  static constexpr int kRawFull = 0, kRawEmpty = 32, kChunkFull = 192, kChunkEmpty = 264, kSFull = 336, kSEmpty = 352,
                        kSentCnt = 368, kSent = 400, kQFull = 440,
                        kQReady = 448, kVtFull = 456, kVtEmpty = 480, kPFull = 504, kPEmpty = 552,
                        kPvDone = 600, kOCorr = 648, kStats = 656, kSentBar = 664, kTmem = 672,
@@ -585,8 +585,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int n_tiles = min(p.tiles_per_split, p.num_tiles - tile0);
   const int n_pc = kPiecesPerTile * n_tiles;  // 32-row stages / pieces of this unit
 
-  // The resolve warp's first global loads (sequence, length, the first four
-  // stages' top-k slots) go out before the set-up, so their latency overlaps it.
+  // The gather warps' first global loads (sequence, length, the top-k slots of
+  // their first four stages) go out before the set-up, so their latency overlaps it.
   const int32_t b = __ldg(p.q_seq + t);
   const int32_t len = (b >= 0 && b < p.num_seqs) ? __ldg(p.seq_lens + b) : 0;
   const int32_t* idx_row = p.topk_idx + static_cast<int64_t>(t) * p.topk;
@@ -594,10 +594,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int slot = tile0 * kTile + u * kSub + lane;
     return (u < n_pc && slot < p.topk) ? __ldg(idx_row + slot) : -1;
   };
-  int32_t posa[4];
-  if (warp == kProducerWarp) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) posa[k] = load_pos(k);
+  const int gw = warp - kGatherWarp;  // gather warp gw takes stages gw, gw + 2, gw + 4, ...
+  int32_t pos0 = -1, pos1 = -1, pos2 = -1, pos3 = -1;  // top-k slots of its next four stages
+  if (gw == 0 || gw == 1) {
+    pos0 = load_pos(gw);
+    pos1 = load_pos(gw + 2);
+    pos2 = load_pos(gw + 4);
+    pos3 = load_pos(gw + 6);
   }
 
   auto bar = [&](int off, int i) { return ctl + off + 8u * static_cast<uint32_t>(i); };
@@ -609,10 +612,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(Ctl::kRawFull, s), 1);  // armed with the stage's bytes, then the copies
       mbar_init(bar(Ctl::kRawEmpty, s), rank == 0 ? 2 : 8);
       st_shared_u32(ctl + Ctl::kLastStage + 4 * s, 0u);
-    }
-    for (int s = 0; s < L::kOffsSlots; ++s) {
-      mbar_init(bar(Ctl::kOffsFull, s), 1);
-      mbar_init(bar(Ctl::kOffsEmpty, s), 1);
     }
     for (int s = 0; s < L::kKSlots; ++s) {
       mbar_init(bar(Ctl::kChunkFull, s), 4);  // the four quadrant warps of one dequant set
@@ -670,119 +669,94 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto raw_row = [&](int s, int r) {  // row r (0..31) of gather stage s
     return raw_base + s * stage_bytes + (r >> 2) * group_bytes + (r & 3) * row_pad;
   };
-  const uint32_t offs_base = sbase + (rank == 0 ? L::kOffsS : L::kOffsO);
-  auto offs_row = [&](int slot) { return offs_base + slot * L::kOffsSlot; };
-  auto offs_mask = [&](int slot) { return offs_base + slot * L::kOffsSlot + kSub * 8; };
-  auto mask_of = [&](int u) {  // live-row mask of stage u (published by the resolve warp)
+  auto mask_of = [&](int u) {  // live-row mask of stage u (published by its gather warp)
     return *reinterpret_cast<volatile uint32_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31));
   };
 
-  if (warp == kGatherWarp) {
-    // ------------------------------------------------ gather copies (one warp, whole stages)
-    // Stage u: lanes 0-7 issue the gather4 copies of row groups 0-7 (a group
+  if (gw == 0 || gw == 1) {
+    // ------------------------------------------------ resolve + gather (two warps, alternate stages)
+    // A copy instruction is accepted only every hundred or more cycles and the
+    // slot -> page -> row chain is two dependent global loads, so two warps
+    // share the stages: warp 6 the even ones, warp 7 the odd ones. Lane j
+    // resolves slot j of the stage; the block-table loads run two of the
+    // warp's stages ahead and the index loads four. Each stage has its own
+    // barrier pair, so the two warps never share one. Stage u: the live-row
+    // mask goes to the mask ring, the barrier is armed with the stage's byte
+    // count, and lanes 0-7 issue the gather4 copies of row groups 0-7 (a group
     // with no live row is skipped; dead rows of a live group re-read one of
     // its live rows). Fallback (a page stride that is not a whole number of
-    // rows): lane j copies row j when live. The stage's barrier is armed with
-    // its byte count before the copies, and the last use of each stage is
-    // recorded for the drain at teardown.
-    const CUtensorMap* tmap = rank == 0 ? &tm_s : &tm_o;
-    const uint32_t copy = rank == 0 ? static_cast<uint32_t>(L::kRowS)
-                                    : static_cast<uint32_t>(L::kCopyO);
-    for (int u = 0; u < n_pc; ++u) {
-      const int os = u % L::kOffsSlots;
-      const int s = u % stages;  // data slot
-      if (!warp_wait(bar(Ctl::kOffsFull, os), (u / L::kOffsSlots) & 1u, abort_addr, lim)) break;
-      if (u >= stages) {  // data slot s is free once stage u - stages was released
-        const int v = u - stages;
-        if (!warp_wait(bar(Ctl::kRawEmpty, v % kRawBars), (v / kRawBars) & 1u, abort_addr, lim))
-          break;
-      }
-      const uint32_t mask = static_cast<uint32_t>(ld_shared_u64(offs_mask(os)));
-      const uint32_t full = bar(Ctl::kRawFull, u % kRawBars);
-      if (p.use_tma) {
-        const uint32_t any = (mask | (mask >> 1) | (mask >> 2) | (mask >> 3)) & 0x11111111u;
-        if (lane == 0) mbar_arrive_tx(full, static_cast<uint32_t>(__popc(any)) * 4u * row_pad);
-        __syncwarp();
-        if (lane < kSub / 4) {
-          const uint32_t m4 = (mask >> (4 * lane)) & 15u;
-          if (m4 != 0u) {
-            const int first = 4 * lane + __ffs(m4) - 1;
-            int32_t y[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int r = ((m4 >> k) & 1u) ? 4 * lane + k : first;
-              y[k] = static_cast<int32_t>(ld_shared_u64(offs_row(os) + 8 * r) / L::kRowBytes);
-            }
-            gather4(raw_row(s, 4 * lane), tmap, y[0], y[1], y[2], y[3], full);
-          }
-        }
-      } else {
-        if (lane == 0) mbar_arrive_tx(full, static_cast<uint32_t>(__popc(mask)) * copy);
-        __syncwarp();
-        if ((mask >> lane) & 1u)
-          bulk_g2s(raw_row(s, lane), p.cache + ld_shared_u64(offs_row(os) + 8 * lane), copy, full);
-      }
-      __syncwarp();
-      if (lane == 0) {
-        st_shared_u32(ctl + Ctl::kLastStage + 4 * (u % kRawBars), static_cast<uint32_t>(u + 1));
-        mbar_arrive(bar(Ctl::kOffsEmpty, os));
-      }
-    }
-  } else if (warp == kProducerWarp) {
-    // ------------------------------------------------ resolve: slots -> row offsets
-    // Index and block-table loads are dependent global loads; four stages are
-    // resolved per batch with all their loads in flight together, and the
-    // next batch's index loads overlap this batch's block-table loads.
+    // rows): lane j copies row j when live. The last use of each barrier pair
+    // is recorded for the drain at teardown.
     const bool seq_ok = b >= 0 && b < p.num_seqs;
     const int32_t* bt_row = p.block_table + static_cast<int64_t>(seq_ok ? b : 0) * p.max_blocks;
+    const bool pow2 = (p.page_size & (p.page_size - 1)) == 0;
+    const int psh = __ffs(p.page_size) - 1;
+    auto page_of = [&](int32_t ps) { return pow2 ? ps >> psh : ps / p.page_size; };
+    auto in_page = [&](int32_t ps) { return pow2 ? ps & (p.page_size - 1) : ps % p.page_size; };
     // page of a position: >= 0, -1 for an empty slot, -2 when it does not
     // resolve. The block-table load is issued before the length check (its
     // index is kept inside the sequence's row), so it does not wait on the
     // length load.
     auto load_page = [&](int32_t ps) -> int64_t {
-      const int32_t pi = ps >= 0 ? ps / p.page_size : -1;
+      const int32_t pi = ps >= 0 ? page_of(ps) : -1;
       const bool in_row = seq_ok && pi >= 0 && pi < p.max_blocks;
       const int64_t e = in_row ? __ldg(bt_row + pi) : -1;
       return ps == -1 ? -1 : (!in_row || ps >= len || e < 0 || e >= p.num_blocks) ? -2 : e;
     };
-    bool stop = false;
-    for (int u0 = 0; u0 < n_pc && !stop; u0 += 4) {
-      int64_t pg[4];
-      int32_t posb[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) pg[k] = load_page(posa[k]);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) posb[k] = load_pos(u0 + 4 + k);
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int u = u0 + k;
-        if (u >= n_pc) break;
-        const int os = u % L::kOffsSlots;
-        if (!warp_wait(bar(Ctl::kOffsEmpty, os), ((u / L::kOffsSlots) & 1u) ^ 1u, abort_addr,
-                       lim)) {
-          stop = true;
+    const CUtensorMap* tmap = rank == 0 ? &tm_s : &tm_o;
+    const uint32_t copy = rank == 0 ? static_cast<uint32_t>(L::kRowS)
+                                    : static_cast<uint32_t>(L::kCopyO);
+    const int64_t rows_per_page = p.block_stride / L::kRowBytes;  // whole rows (tensor-map path)
+    int64_t pg0 = load_page(pos0), pg1 = load_page(pos1);
+    for (int u = gw; u < n_pc; u += 2) {
+      const int64_t pg2 = load_page(pos2);          // stage u + 4
+      const int32_t pos4 = load_pos(u + 8);         // stage u + 8
+      const bool val = pg0 >= 0;
+      const uint32_t mask = __ballot_sync(0xffffffffu, val);
+      if (rank == 0) {
+        const int bad = __popc(__ballot_sync(0xffffffffu, pg0 == -2));
+        if (lane == 0 && bad > 0 && p.invalid_count != nullptr) atomicAdd(p.invalid_count, bad);
+      }
+      const int s = u % stages;  // data slot
+      if (u >= stages) {  // data slot s is free once stage u - stages was released
+        const int v = u - stages;
+        if (!warp_wait(bar(Ctl::kRawEmpty, v % kRawBars), (v / kRawBars) & 1u, abort_addr, lim))
           break;
-        }
-        const bool val = pg[k] >= 0;
-        const int64_t off =
-            val ? pg[k] * p.block_stride + static_cast<int64_t>(posa[k] % p.page_size) * L::kRowBytes
-                : 0;
-        st_shared_u64(offs_row(os) + 8 * lane, static_cast<uint64_t>(off));
-        const uint32_t mask = __ballot_sync(0xffffffffu, val);
-        if (rank == 0) {
-          const int bad = __popc(__ballot_sync(0xffffffffu, pg[k] == -2));
-          if (lane == 0 && bad > 0 && p.invalid_count != nullptr) atomicAdd(p.invalid_count, bad);
-        }
+      }
+      const uint32_t full = bar(Ctl::kRawFull, u % kRawBars);
+      // the mask is stored before the arrive (release) that the dequant warps acquire
+      if (lane == 0)
+        *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31)) = mask;
+      if (p.use_tma) {
+        const uint32_t any = (mask | (mask >> 1) | (mask >> 2) | (mask >> 3)) & 0x11111111u;
+        if (lane == 0) mbar_arrive_tx(full, static_cast<uint32_t>(__popc(any)) * 4u * row_pad);
+        const int32_t row = val ? static_cast<int32_t>(pg0 * rows_per_page + in_page(pos0)) : 0;
+        const int g = lane & 7;
+        const uint32_t m4 = (mask >> (4 * g)) & 15u;
+        const int first = m4 != 0u ? 4 * g + __ffs(m4) - 1 : 0;
+        int32_t y[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          y[k] = __shfl_sync(0xffffffffu, row, ((m4 >> k) & 1u) ? 4 * g + k : first);
+        if (lane < kSub / 4 && m4 != 0u)
+          gather4(raw_row(s, 4 * lane), tmap, y[0], y[1], y[2], y[3], full);
+      } else {
+        if (lane == 0) mbar_arrive_tx(full, static_cast<uint32_t>(__popc(mask)) * copy);
         __syncwarp();
-        if (lane == 0) {
-          st_shared_u64(offs_mask(os), mask);
-          *reinterpret_cast<volatile uint64_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31)) =
-              mask;
-          mbar_arrive(bar(Ctl::kOffsFull, os));
+        if (val) {
+          const int64_t off = pg0 * p.block_stride + static_cast<int64_t>(in_page(pos0)) * L::kRowBytes;
+          bulk_g2s(raw_row(s, lane), p.cache + off, copy, full);
         }
       }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) posa[k] = posb[k];
+      __syncwarp();
+      if (lane == 0)
+        st_shared_u32(ctl + Ctl::kLastStage + 4 * (u % kRawBars), static_cast<uint32_t>(u + 1));
+      pos0 = pos1;
+      pos1 = pos2;
+      pos2 = pos3;
+      pos3 = pos4;
+      pg0 = pg1;
+      pg1 = pg2;
     }
   } else if (warp >= kDequantWarp0 && rank == 0) {
     // ------------------------------------------------ score CTA: rows -> K chunks in TMEM
