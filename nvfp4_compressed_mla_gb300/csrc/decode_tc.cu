@@ -195,6 +195,18 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
   return ok != 0;
 }
+// Non-blocking phase test (never suspends the thread).
+__device__ __forceinline__ bool mbar_ready(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
   uint32_t v;
   asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
@@ -946,6 +958,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // descriptor's address field counts 16 bytes.
           const uint64_t qd = sw128_desc(sbase + L::kQ);
           bool run = true;
+          // Whether chunk q is known to be in the ring: the next chunk's
+          // barrier is tested (without blocking) before this chunk's MMAs go
+          // out, so a chunk that is already there costs no wait at all.
+          bool ready = false;
           for (int i = 0; i < n_tiles && run; ++i) {
             const int s2 = i % L::kSBufs;
             const uint32_t sph = static_cast<uint32_t>(i / L::kSBufs) & 1u;
@@ -954,11 +970,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (int kb = 0; kb < kChunksPerTile; ++kb) {
               const int q = kChunksPerTile * i + kb;
               const int cs = q % L::kKSlots;
-              if (!wait_bar(bar(Ctl::kChunkFull, cs), (q / L::kKSlots) & 1u, abort_addr, lim)) {
+              if (!ready &&
+                  !wait_bar(bar(Ctl::kChunkFull, cs), (q / L::kKSlots) & 1u, abort_addr, lim)) {
                 run = false;
                 break;
               }
               tc_fence_after();
+              ready = mbar_ready(bar(Ctl::kChunkFull, (q + 1) % L::kKSlots),
+                                 ((q + 1) / L::kKSlots) & 1u);
               const uint64_t bd = qd + static_cast<uint64_t>(kb * (L::kQTile >> 4));
               const uint32_t a = 32u * static_cast<uint32_t>(cs);
 #pragma unroll
