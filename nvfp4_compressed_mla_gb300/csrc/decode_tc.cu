@@ -55,7 +55,11 @@ constexpr int kSub = 32;                     // rows per gather stage / P piece 
 constexpr int kPiecesPerTile = kTile / kSub;  // 4
 constexpr int kWarps = 16;
 constexpr int kThreads = kWarps * 32;
-constexpr int kMmaWarp = 5, kGatherWarp = 6;  // gather warps 6 and 7; warp 4 has no role
+constexpr int kMmaWarp = 5, kGatherWarp = 6;  // gather warps 6 and 7
+constexpr int kQWarp = 4;                     // score CTA: helps convert Q
+// Score CTA: Q is converted by the softmax warps 0-3, warp 4 and the dequant
+// warps 8-15 (idle until their first rows land).
+constexpr int kQConverters = 13;
 constexpr int kDequantWarp0 = 8;             // warps 8..15; warp w runs on sub-partition w % 4
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunksPerTile = 9;            // 8 latent chunks + the rope chunk
@@ -647,7 +651,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(bar(Ctl::kPvDone, s), 1);
     }
     mbar_init(bar(Ctl::kQFull, 0), 1);
-    mbar_init(bar(Ctl::kQReady, 0), 4);
+    mbar_init(bar(Ctl::kQReady, 0), kQConverters);
     mbar_init(bar(Ctl::kOCorr, 0), 128);
     mbar_init(bar(Ctl::kStats, 0), 128);
     mbar_init(bar(Ctl::kSentBar, 0), 1);
@@ -683,6 +687,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
   auto mask_of = [&](int u) {  // live-row mask of stage u (published by its gather warp)
     return *reinterpret_cast<volatile uint32_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31));
+  };
+  // Score CTA: converter g (0..415) turns its share of Q (bf16, as loaded)
+  // into FP16 in place, scales folded in, heads >= H zeroed: 16-byte item i =
+  // g + 416 k is chunk i % 8 of head (i / 8) % 128 of tile i / 1024 (a quarter
+  // warp covers one 128-byte row: no bank conflicts). Then the warp signals
+  // QReady. A warp whose wait for the Q copies failed converts nothing.
+  auto convert_q = [&](int g) {
+    const bool qok = warp_wait(bar(Ctl::kQFull, 0), 0, abort_addr, lim);
+    if (qok) {
+      constexpr int kItems = kChunksPerTile * 128 * 8;
+#pragma unroll 1
+      for (int i = g; i < kItems; i += 32 * kQConverters) {
+        const int kb = i >> 10, h = (i >> 3) & 127, c = i & 7;
+        const float m = kb < 8 ? p.q_lat_mult : p.q_rope_mult;
+        const uint32_t a = sbase + L::kQ + kb * L::kQTile +
+                           sw128_off(static_cast<uint32_t>(h), static_cast<uint32_t>(c));
+        const uint4 x = h < p.num_heads ? bf16x8_to_f16x8(ld_shared_v4(a), m)
+                                        : make_uint4(0u, 0u, 0u, 0u);
+        st_shared_v4(a, x.x, x.y, x.z, x.w);
+      }
+    }
+    fence_proxy_async_cta();  // generic stores -> visible to the MMA's operand reads
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar(Ctl::kQReady, 0));
   };
 
   if (gw == 0 || gw == 1) {
@@ -770,6 +798,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       pg0 = pg1;
       pg1 = pg2;
     }
+  } else if (warp == kQWarp && rank == 0) {
+    convert_q(128 + lane);
   } else if (warp >= kDequantWarp0 && rank == 0) {
     // ------------------------------------------------ score CTA: rows -> K chunks in TMEM
     // Warp (set, quadrant) = ((w - 8) / 4, w % 4) expands, for every tile i,
@@ -780,6 +810,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // rows are written as zeros. NVFP4 rows: each thread first loads its
     // whole share into registers and releases the gather stage, so a tile's
     // four stages never wait on one another.
+    convert_q(160 + 32 * (warp - kDequantWarp0) + lane);
     const int quad = warp & 3;
     const int set = (warp - kDequantWarp0) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
@@ -1031,28 +1062,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
     bool ok;
     {
-      // Q (bf16) of this token: thread = head h converts its row in place to
-      // FP16 (scales folded in; heads >= H zeroed); also the ones matrix and
-      // the initial reference maxima.
-      const int h = tid;
-      ok = group_and(wait_bar(bar(Ctl::kQFull, 0), 0, abort_addr, lim));
-      const bool live = ok && h < p.num_heads;
-#pragma unroll 1
-      for (int kb = 0; kb < kChunksPerTile; ++kb) {
-        const float m = kb < 8 ? p.q_lat_mult : p.q_rope_mult;
-        const uint32_t tile = sbase + L::kQ + kb * L::kQTile;
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          const uint32_t a = tile + sw128_off(static_cast<uint32_t>(h), c);
-          const uint4 x = live ? bf16x8_to_f16x8(ld_shared_v4(a), m) : make_uint4(0u, 0u, 0u, 0u);
-          st_shared_v4(a, x.x, x.y, x.z, x.w);
-        }
-      }
-      st_shared_u32(sbase + L::kNegM + 4 * h, __float_as_uint(INFINITY));  // m_ref = -inf
-      fence_proxy_async_cta();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar(Ctl::kQReady, 0));
-      group_sync();  // every head's reference maximum is initialised
+      // this warp's share of Q, then the initial reference maxima
+      st_shared_u32(sbase + L::kNegM + 4 * tid, __float_as_uint(INFINITY));  // m_ref = -inf
+      convert_q(tid);
+      ok = group_and(ld_shared_u32(abort_addr) == 0u);  // also: every m_ref is initialised
     }
     const float c = p.score_scale;
     const uint64_t c2 = f32x2(c, c);
