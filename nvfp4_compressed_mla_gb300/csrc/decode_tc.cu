@@ -63,7 +63,6 @@ constexpr int kQConverters = 13;
 constexpr int kDequantWarp0 = 8;             // warps 8..15; warp w runs on sub-partition w % 4
 constexpr uint32_t kTmemCols = 512;
 constexpr int kChunksPerTile = 9;            // 8 latent chunks + the rope chunk
-constexpr int kChunksSet0 = 5;               // score dequant: set 0 chunks 0-4, set 1 chunks 5-8
 constexpr int kPBufs = 6;                    // output CTA: P pieces in flight
 constexpr int kVSlots = 3;                   // output CTA: V slots of 32 rows
 // Gather stage u lands in data slot u % stages but completes and is released
@@ -804,18 +803,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ score CTA: rows -> K chunks in TMEM
     // Warp (set, quadrant) = ((w - 8) / 4, w % 4) expands, for every tile i,
     // its share of the 32 rows of stage 4 i + quadrant into TMEM lanes
-    // 32 quadrant .. + 31 (thread = row): set 0 chunks 0-4 (latent dims
-    // 0..319), set 1 chunks 5-8 (dims 320..511 and the rope). Each chunk goes
-    // into the next slot of the K ring once the MMA has released it; dead
-    // rows are written as zeros. NVFP4 rows: each thread first loads its
-    // whole share into registers and releases the gather stage, so a tile's
-    // four stages never wait on one another.
+    // 32 quadrant .. + 31 (thread = row): set 0 the even chunks (latent dims
+    // 0..63, 128..191, 256..319, 384..447) and the rope (chunk 8), set 1 the
+    // odd ones. The MMA takes the chunks in order, so the two sets feed it in
+    // turn and work side by side. Each chunk goes into the next slot of the
+    // K ring once the MMA has released it; dead rows are written as zeros.
+    // NVFP4 rows: each thread first loads its whole share into registers and
+    // releases the gather stage, so a tile's four stages never wait on one
+    // another.
     convert_q(160 + 32 * (warp - kDequantWarp0) + lane);
     const int quad = warp & 3;
     const int set = (warp - kDequantWarp0) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quad) << 16;
-    const int kb0 = set == 0 ? 0 : kChunksSet0;
-    const int kb1 = set == 0 ? kChunksSet0 : kChunksPerTile;
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
     bool run = true;
     for (int i = 0; i < n_tiles && run; ++i) {
@@ -840,32 +839,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         return true;
       };
       if constexpr (L::kNv) {
-        // Row reads stay within bytes [0, 352) of the row slot. Set 0 keeps the
-        // codes of its five chunks (dims 0..319, 10 x 16 B) and their scale
-        // words; set 1 those of chunks 5-7 (dims 320..511, 6 x 16 B) and the
-        // rope (4 x 16 B). The loop is rolled (one copy of the conversion
+        // Row reads stay within bytes [0, 352) of the row slot. Each set keeps
+        // the codes of its four latent chunks (2 x 16 B each, at byte 32 kb)
+        // and their scale words (word kb of the 32 scale bytes); set 0 also
+        // the rope (4 x 16 B). The loop is rolled (one copy of the conversion
         // code): each chunk takes cw[0], cw[1] and scw[0], then both shift.
-        uint4 cw[10];
-        uint32_t scw[5];
+        uint4 cw[8], rp[4];
+        uint32_t scw[4];
         {
           const uint4 s0 = ok ? ld_shared_v4(src + kScaleOff) : z;
           const uint4 s1 = ok ? ld_shared_v4(src + kScaleOff + 16) : z;
-          scw[0] = set == 0 ? s0.x : s1.y;
-          scw[1] = set == 0 ? s0.y : s1.z;
-          scw[2] = set == 0 ? s0.z : s1.w;
-          scw[3] = set == 0 ? s0.w : 0u;
-          scw[4] = set == 0 ? s1.x : 0u;
+          scw[0] = set == 0 ? s0.x : s0.y;
+          scw[1] = set == 0 ? s0.z : s0.w;
+          scw[2] = set == 0 ? s1.x : s1.y;
+          scw[3] = set == 0 ? s1.z : s1.w;
         }
 #pragma unroll
-        for (int x = 0; x < 10; ++x) {
-          const uint32_t a = (set == 0 || x < 6) ? (set == 0 ? 0u : 160u) + 16u * x
-                                                 : static_cast<uint32_t>(kRopeOff) + 16u * (x - 6);
-          cw[x] = ok ? ld_shared_v4(src + a) : z;
-        }
-        const int nlat = set == 0 ? kChunksSet0 : 8 - kChunksSet0;
+        for (int x = 0; x < 8; ++x)
+          cw[x] = ok ? ld_shared_v4(src + 32u * (2u * (x >> 1) + set) + 16u * (x & 1)) : z;
+#pragma unroll
+        for (int x = 0; x < 4; ++x)
+          rp[x] = (ok && set == 0) ? ld_shared_v4(src + kRopeOff + 16u * x) : z;
         uint32_t h[32];
 #pragma unroll 1
-        for (int c = 0; c < nlat && run; ++c) {
+        for (int c = 0; c < 4 && run; ++c) {
           const uint32_t w[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w,
                                  cw[1].x, cw[1].y, cw[1].z, cw[1].w};
           nvfp4_chunk(w, scw[0], h);
@@ -873,27 +870,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, rb));
           }
-          run = put_chunk(kb0 + c, h);
+          run = put_chunk(2 * c + set, h);
 #pragma unroll
-          for (int x = 0; x < 8; ++x) cw[x] = cw[x + 2];
+          for (int x = 0; x < 6; ++x) cw[x] = cw[x + 2];
 #pragma unroll
-          for (int x = 0; x < 4; ++x) scw[x] = scw[x + 1];
+          for (int x = 0; x < 3; ++x) scw[x] = scw[x + 1];
         }
-        if (set == 1 && run) {  // the rope: cw[0..3] after three shifts
+        if (set == 0 && run) {  // the rope
 #pragma unroll
-          for (int x = 0; x < 4; ++x) e4m3x16_to_f16(cw[x], h + 8 * x);
+          for (int x = 0; x < 4; ++x) e4m3x16_to_f16(rp[x], h + 8 * x);
           run = put_chunk(kChunksPerTile - 1, h);
         }
       } else {
         // FP8 rows: chunk by chunk from shared memory (the K ring holds a
-        // whole tile, so no chunk waits on another stage)
+        // whole tile, so no chunk waits on another stage); set 0 the even
+        // chunks 0-8, set 1 the odd ones
+        const int kb_last = set == 0 ? kChunksPerTile - 1 : kChunksPerTile - 2;
 #pragma unroll 1
-        for (int kb = kb0; kb < kb1 && run; ++kb) {
+        for (int kb = set; kb < kChunksPerTile && run; kb += 2) {
           uint32_t h[32];
 #pragma unroll
           for (int x = 0; x < 4; ++x)
             e4m3x16_to_f16(ok ? ld_shared_v4(src + 64 * kb + 16 * x) : z, h + 8 * x);
-          if (kb == kb1 - 1) {
+          if (kb == kb_last) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, rb));
           }
