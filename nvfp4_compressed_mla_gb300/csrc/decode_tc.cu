@@ -62,7 +62,12 @@ constexpr int kQWarp = 4;                     // score CTA: helps convert Q
 constexpr int kQConverters = 13;
 constexpr int kDequantWarp0 = 8;             // warps 8..15; warp w runs on sub-partition w % 4
 constexpr uint32_t kTmemCols = 512;
-constexpr int kChunksPerTile = 9;            // 8 latent chunks + the rope chunk
+constexpr int kQTiles = 9;                   // Q: 8 latent 64-dim tiles + the rope tile
+// K ring chunks per 128-row tile: 4 latent chunks of 128 dims (64 TMEM
+// columns, 8 MMAs each) and the rope (64 dims, 4 MMAs). Large chunks keep the
+// single MMA-issuing thread's per-chunk handshake (barrier test, fence,
+// commit) off the tensor pipe's critical path.
+constexpr int kChunksPerTile = 5;
 constexpr int kPBufs = 6;                    // output CTA: P pieces in flight
 constexpr int kVSlots = 3;                   // output CTA: V slots of 32 rows
 // Gather stage u lands in data slot u % stages but completes and is released
@@ -94,14 +99,12 @@ struct TcLayout {
   static constexpr int kRowBytes = kNv ? kNvfp4Row : kFp8Row;
   static constexpr int kElem = kNv ? 2 : 4;                 // tensor-map element bytes
   static constexpr int kRowElems = kRowBytes / kElem;       // 176 / 144
-  // Tensor memory of the score CTA: K ring (32 columns per 64-dim chunk),
-  // then the S^T buffers (128 columns each). NVFP4: 8 ring slots and two
-  // S^T buffers; FP8 rows (too wide to hold in registers) get a ring for a
-  // whole tile and one S^T buffer.
-  static constexpr int kKSlots = kNv ? 8 : 9;
-  static constexpr int kSBufs = kNv ? 2 : 1;
-  static constexpr uint32_t kSCol = kNv ? 256u : 384u;
-  static_assert(32u * kKSlots <= kSCol && kSCol + 128u * kSBufs <= kTmemCols,
+  // Tensor memory of the score CTA: K ring (4 slots of 64 columns, one
+  // 128-dimension chunk each), then two S^T buffers (128 columns each).
+  static constexpr int kKSlots = 4;
+  static constexpr int kSBufs = 2;
+  static constexpr uint32_t kSCol = 256u;
+  static_assert(64u * kKSlots <= kSCol && kSCol + 128u * kSBufs <= kTmemCols,
                 "tensor memory plan");
   // Gathered rows, four per tensor copy; groups start 128-byte aligned.
   // Score CTA: whole rows. Output CTA: the latent part (NVFP4: codes and
@@ -119,7 +122,7 @@ struct TcLayout {
   // score CTA
   static constexpr int kQTile = 16384;                      // 128 heads x 64 dims (SW128)
   static constexpr int kQ = 0;                              // 9 tiles: 8 latent + rope
-  static constexpr int kRawS = kQ + kChunksPerTile * kQTile;
+  static constexpr int kRawS = kQ + kQTiles * kQTile;
   static constexpr int kStg = kRawS + kStagesS * kStageS;   // 4 P^T staging slots
   static constexpr int kNegM = kStg + kPiecesPerTile * kPiece;  // -(reference maximum) per head
   static constexpr int kAlpha = kNegM + 512;                // rescale factor per head
@@ -670,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   // copies into 128-byte-swizzled tiles, the layout of the MMA's B operand.
   if (rank == 0 && tid == 32) {
     const uint32_t qbar = bar(Ctl::kQFull, 0);
-    mbar_arrive_tx(qbar, static_cast<uint32_t>(kChunksPerTile * L::kQTile));
+    mbar_arrive_tx(qbar, static_cast<uint32_t>(kQTiles * L::kQTile));
     const int32_t y = t * p.num_heads;
     for (int kb = 0; kb < 8; ++kb)
       tma_load_2d(sbase + L::kQ + kb * L::kQTile, &tm_ql, 64 * kb, y, qbar);
@@ -695,7 +698,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto convert_q = [&](int g) {
     const bool qok = warp_wait(bar(Ctl::kQFull, 0), 0, abort_addr, lim);
     if (qok) {
-      constexpr int kItems = kChunksPerTile * 128 * 8;
+      constexpr int kItems = kQTiles * 128 * 8;
 #pragma unroll 1
       for (int i = g; i < kItems; i += 32 * kQConverters) {
         const int kb = i >> 10, h = (i >> 3) & 127, c = i & 7;
@@ -803,14 +806,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ score CTA: rows -> K chunks in TMEM
     // Warp (set, quadrant) = ((w - 8) / 4, w % 4) expands, for every tile i,
     // its share of the 32 rows of stage 4 i + quadrant into TMEM lanes
-    // 32 quadrant .. + 31 (thread = row): set 0 the even chunks (latent dims
-    // 0..63, 128..191, 256..319, 384..447) and the rope (chunk 8), set 1 the
-    // odd ones. The MMA takes the chunks in order, so the two sets feed it in
-    // turn and work side by side. Each chunk goes into the next slot of the
-    // K ring once the MMA has released it; dead rows are written as zeros.
-    // NVFP4 rows: each thread first loads its whole share into registers and
-    // releases the gather stage, so a tile's four stages never wait on one
-    // another.
+    // 32 quadrant .. + 31 (thread = row): set 0 the latent chunks 0 and 2
+    // (dims 0..127, 256..383) and the rope (chunk 4), set 1 the latent chunks
+    // 1 and 3. The MMA takes the chunks in order, so the two sets feed it in
+    // turn and work side by side. A chunk goes into the next slot of the K
+    // ring once the MMA has released it, in 64-dimension halves (32 columns
+    // each; a half's store completes before its registers are reused); dead
+    // rows are written as zeros. NVFP4 rows: each thread first loads its
+    // whole share into registers and releases the gather stage, so a tile's
+    // four stages never wait on one another.
     convert_q(160 + 32 * (warp - kDequantWarp0) + lane);
     const int quad = warp & 3;
     const int set = (warp - kDequantWarp0) >> 2;
@@ -824,79 +828,101 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (!warp_wait(bar(Ctl::kRawFull, rb), (u / kRawBars) & 1u, abort_addr, lim)) break;
       const bool ok = (mask_of(u) >> lane) & 1u;
       const uint32_t src = raw_row(s, lane);
-      // one chunk: wait for its ring slot, store 32 columns, signal the MMA
-      auto put_chunk = [&](int kb, const uint32_t (&h)[32]) -> bool {
-        const int q = kChunksPerTile * i + kb;
+      // the ring slot of chunk c of this tile, once the MMA has released it
+      auto take_slot = [&](int c, uint32_t& col) -> bool {
+        const int q = kChunksPerTile * i + c;
         const int cs = q % L::kKSlots;
+        col = 64u * static_cast<uint32_t>(cs);
         if (!warp_wait(bar(Ctl::kChunkEmpty, cs), ((q / L::kKSlots) & 1u) ^ 1u, abort_addr, lim))
           return false;
         tc_fence_after();
-        tmem_st32(tmem + lane_base + 32u * static_cast<uint32_t>(cs), h);
+        return true;
+      };
+      // 32 columns into TMEM, complete before the registers are reused
+      auto put_half = [&](uint32_t c0, const uint32_t (&h)[32]) {
+        tmem_st32(tmem + lane_base + c0, h);
         tmem_st_wait();
+      };
+      auto chunk_done = [&](int c) {
+        const int cs = (kChunksPerTile * i + c) % L::kKSlots;
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bar(Ctl::kChunkFull, cs));
-        return true;
       };
+      uint32_t col = 0;
       if constexpr (L::kNv) {
         // Row reads stay within bytes [0, 352) of the row slot. Each set keeps
-        // the codes of its four latent chunks (2 x 16 B each, at byte 32 kb)
-        // and their scale words (word kb of the 32 scale bytes); set 0 also
-        // the rope (4 x 16 B). The loop is rolled (one copy of the conversion
-        // code): each chunk takes cw[0], cw[1] and scw[0], then both shift.
+        // the codes of its two latent chunks (4 x 16 B each, at byte 64 c) and
+        // their four scale words (words 2 c, 2 c + 1); set 0 also the rope
+        // (4 x 16 B). The loop is rolled over the four 64-dimension halves
+        // (one copy of the conversion code): each takes cw[0], cw[1] and
+        // scw[0], then both shift.
         uint4 cw[8], rp[4];
         uint32_t scw[4];
         {
           const uint4 s0 = ok ? ld_shared_v4(src + kScaleOff) : z;
           const uint4 s1 = ok ? ld_shared_v4(src + kScaleOff + 16) : z;
-          scw[0] = set == 0 ? s0.x : s0.y;
-          scw[1] = set == 0 ? s0.z : s0.w;
-          scw[2] = set == 0 ? s1.x : s1.y;
-          scw[3] = set == 0 ? s1.z : s1.w;
+          scw[0] = set == 0 ? s0.x : s0.z;
+          scw[1] = set == 0 ? s0.y : s0.w;
+          scw[2] = set == 0 ? s1.x : s1.z;
+          scw[3] = set == 0 ? s1.y : s1.w;
         }
 #pragma unroll
         for (int x = 0; x < 8; ++x)
-          cw[x] = ok ? ld_shared_v4(src + 32u * (2u * (x >> 1) + set) + 16u * (x & 1)) : z;
+          cw[x] = ok ? ld_shared_v4(src + 64u * (2u * (x >> 2) + set) + 16u * (x & 3)) : z;
 #pragma unroll
         for (int x = 0; x < 4; ++x)
           rp[x] = (ok && set == 0) ? ld_shared_v4(src + kRopeOff + 16u * x) : z;
         uint32_t h[32];
 #pragma unroll 1
-        for (int c = 0; c < 4 && run; ++c) {
+        for (int j = 0; j < 4 && run; ++j) {
           const uint32_t w[8] = {cw[0].x, cw[0].y, cw[0].z, cw[0].w,
                                  cw[1].x, cw[1].y, cw[1].z, cw[1].w};
           nvfp4_chunk(w, scw[0], h);
-          if (c == 0) {  // the share is in registers: the gather warp may refill the stage
+          if (j == 0) {  // the share is in registers: the gather warp may refill the stage
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, rb));
           }
-          run = put_chunk(2 * c + set, h);
+          const int c = set + 2 * (j >> 1);  // chunk of this half
+          if ((j & 1) == 0) run = take_slot(c, col);
+          if (!run) break;
+          put_half(col + 32u * static_cast<uint32_t>(j & 1), h);
+          if (j & 1) chunk_done(c);
 #pragma unroll
           for (int x = 0; x < 6; ++x) cw[x] = cw[x + 2];
 #pragma unroll
           for (int x = 0; x < 3; ++x) scw[x] = scw[x + 1];
         }
-        if (set == 0 && run) {  // the rope
+        if (set == 0 && run) {  // the rope: chunk 4, 32 of its slot's columns
 #pragma unroll
           for (int x = 0; x < 4; ++x) e4m3x16_to_f16(rp[x], h + 8 * x);
-          run = put_chunk(kChunksPerTile - 1, h);
+          run = take_slot(kChunksPerTile - 1, col);
+          if (run) {
+            put_half(col, h);
+            chunk_done(kChunksPerTile - 1);
+          }
         }
       } else {
-        // FP8 rows: chunk by chunk from shared memory (the K ring holds a
-        // whole tile, so no chunk waits on another stage); set 0 the even
-        // chunks 0-8, set 1 the odd ones
-        const int kb_last = set == 0 ? kChunksPerTile - 1 : kChunksPerTile - 2;
+        // FP8 rows: half by half from shared memory; set 0 the chunks 0, 2 and
+        // the rope (bytes 512..575), set 1 the chunks 1 and 3; the stage is
+        // released after the set's last read of it
+        const int nhalf = set == 0 ? 5 : 4;
 #pragma unroll 1
-        for (int kb = set; kb < kChunksPerTile && run; kb += 2) {
+        for (int j = 0; j < nhalf && run; ++j) {
+          const int c = j < 4 ? set + 2 * (j >> 1) : kChunksPerTile - 1;
+          const uint32_t off = 128u * static_cast<uint32_t>(c) + 64u * static_cast<uint32_t>(j & 1);
           uint32_t h[32];
 #pragma unroll
           for (int x = 0; x < 4; ++x)
-            e4m3x16_to_f16(ok ? ld_shared_v4(src + 64 * kb + 16 * x) : z, h + 8 * x);
-          if (kb == kb_last) {
+            e4m3x16_to_f16(ok ? ld_shared_v4(src + off + 16 * x) : z, h + 8 * x);
+          if (j == nhalf - 1) {
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(Ctl::kRawEmpty, rb));
           }
-          run = put_chunk(kb, h);
+          if ((j & 1) == 0) run = take_slot(c, col);
+          if (!run) break;
+          put_half(col + 32u * static_cast<uint32_t>(j & 1), h);
+          if ((j & 1) || j == 4) chunk_done(c);
         }
       }
     }
@@ -1008,11 +1034,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               tc_fence_after();
               ready = mbar_ready(bar(Ctl::kChunkFull, (q + 1) % L::kKSlots),
                                  ((q + 1) / L::kKSlots) & 1u);
-              const uint64_t bd = qd + static_cast<uint64_t>(kb * (L::kQTile >> 4));
-              const uint32_t a = 32u * static_cast<uint32_t>(cs);
+              // chunk kb < 4: Q tiles 2 kb and 2 kb + 1 (8 MMAs); the rope: Q tile 8
+              const uint64_t bd = qd + static_cast<uint64_t>(2 * kb * (L::kQTile >> 4));
+              const uint32_t a = 64u * static_cast<uint32_t>(cs);
+              const int nk = kb < kChunksPerTile - 1 ? 8 : 4;
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(dcol, a + 8u * kk, bd + 2u * kk, kIdescQK, (kb | kk) != 0 ? 1u : 0u);
+              for (int kk = 0; kk < 8; ++kk)
+                if (kk < nk)
+                  mma_ts(dcol, a + 8u * kk,
+                         bd + static_cast<uint64_t>((kk >> 2) * (L::kQTile >> 4) + 2 * (kk & 3)),
+                         kIdescQK, (kb | kk) != 0 ? 1u : 0u);
               mma_commit(bar(Ctl::kChunkEmpty, cs));
               last_bar = bar(Ctl::kChunkEmpty, cs);
               last_parity = (q / L::kKSlots) & 1u;
