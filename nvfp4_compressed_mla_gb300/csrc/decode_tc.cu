@@ -151,7 +151,7 @@ struct TcLayout {
 struct Ctl {
   static constexpr int kRawFull = 0, kRawEmpty = 32, kChunkFull = 192, kChunkEmpty = 264, kSFull = 336, kSEmpty = 352,
                        kSentCnt = 368, kSent = 400, kQFull = 440,
-                       kQReady = 448, kVtFull = 456, kVtEmpty = 480, kPFull = 504, kPEmpty = 552,
+                       kQReady = 448, kVtFull = 456, kPFull = 504, kPEmpty = 552,
                        kPvDone = 600, kOCorr = 648, kStats = 656, kSentBar = 664, kTmem = 672,
                        kAbort = 676, kLastStage = 688, kMaskRing = 704,
                        kEnd = 960;
@@ -201,16 +201,27 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
   return ok != 0;
 }
-// Non-blocking phase test (never suspends the thread).
+// Non-blocking phase test (never suspends the thread); cluster-scope acquire
+// for barriers that the peer CTA arrives on.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_ready(uint32_t bar, uint32_t parity) {
   uint32_t ok;
-  asm volatile(
-      "{\n.reg .pred p;\n"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
-      "selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
+  if constexpr (kCluster)
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+  else
+    asm volatile(
+        "{\n.reg .pred p;\n"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
   return ok != 0;
 }
 __device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
@@ -643,10 +654,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       st_shared_u32(ctl + Ctl::kSentCnt + 4 * s, 0u);
       st_shared_u32(ctl + Ctl::kSent + 4 * s, 0u);
     }
-    for (int s = 0; s < kVSlots; ++s) {
-      mbar_init(bar(Ctl::kVtFull, s), 8);
-      mbar_init(bar(Ctl::kVtEmpty, s), 1);
-    }
+    for (int s = 0; s < kVSlots; ++s) mbar_init(bar(Ctl::kVtFull, s), 8);
     for (int s = 0; s < kPBufs; ++s) {
       mbar_init(bar(Ctl::kPFull, s), 1);
       mbar_init(bar(Ctl::kPEmpty, s), 4);
@@ -932,6 +940,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // slot holds 8 blocks of 64 dims, each block 4 groups of 8 rows x 128 B.
     const int dq = warp - kDequantWarp0;  // 0..7
     bool run = true;
+    // V slot u % 3 is free once the P V MMAs of piece u - 3 have completed
+    // (the one commit per piece, on its P buffer's PvDone barrier)
+    auto v_slot_free = [&](int u) {
+      if (u < kVSlots) return true;
+      const int v = u - kVSlots;
+      return warp_wait(bar(Ctl::kPvDone, v % kPBufs), (v / kPBufs) & 1u, abort_addr, lim);
+    };
     for (int u = 0; u < n_pc && run; ++u) {
       const int s = u % L::kStagesO;   // data slot
       const int rb = u % kRawBars;     // barrier pair
@@ -957,7 +972,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           cd[it] = ok ? ld_shared_v4(rp + 16 * jj[it]) : make_uint4(0u, 0u, 0u, 0u);
           scv[it] = ok ? ld_shared_u16(rp + kScaleOff + 2 * jj[it]) : 0u;
         }
-        if (!warp_wait(bar(Ctl::kVtEmpty, vs), ((u / kVSlots) & 1u) ^ 1u, abort_addr, lim)) break;
+        if (!v_slot_free(u)) break;
 #pragma unroll
         for (int it = 0; it < 2; ++it) {
           const uint32_t s0 = scale_f16x2(scv[it]), s1 = scale_f16x2(scv[it] >> 8);
@@ -978,7 +993,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                          h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
         }
       } else {
-        if (!warp_wait(bar(Ctl::kVtEmpty, vs), ((u / kVSlots) & 1u) ^ 1u, abort_addr, lim)) break;
+        if (!v_slot_free(u)) break;
         const int dt = dq * 32 + lane;
 #pragma unroll
         for (int it = 0; it < 4; ++it) {
@@ -1054,18 +1069,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       } else {
         uint32_t n_corr = 0;
+        // the next piece's P and V barriers are tested (without blocking)
+        // before this piece's MMAs go out
+        bool p_ready = false, v_ready = false;
         for (int u = 0; u < n_pc; ++u) {
           const int pb = u % kPBufs;
           const int vs = u % kVSlots;
           // P (and any rescale of O) first, then the V slot
-          if (!wait_bar<true>(bar(Ctl::kPFull, pb), (u / kPBufs) & 1u, abort_addr, lim)) break;
+          if (!p_ready &&
+              !wait_bar<true>(bar(Ctl::kPFull, pb), (u / kPBufs) & 1u, abort_addr, lim))
+            break;
           const uint4 fl = ld_shared_v4(sbase + L::kAFO + pb * kAFBytes + 512);
           if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
             if (!wait_bar(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr, lim)) break;
             ++n_corr;
           }
-          if (!wait_bar(bar(Ctl::kVtFull, vs), (u / kVSlots) & 1u, abort_addr, lim)) break;
+          if (!v_ready && !wait_bar(bar(Ctl::kVtFull, vs), (u / kVSlots) & 1u, abort_addr, lim))
+            break;
           tc_fence_after();
+          p_ready = mbar_ready<true>(bar(Ctl::kPFull, (u + 1) % kPBufs), ((u + 1) / kPBufs) & 1u);
+          v_ready = mbar_ready(bar(Ctl::kVtFull, (u + 1) % kVSlots), ((u + 1) / kVSlots) & 1u);
           const uint32_t pbuf = sbase + L::kP + pb * kPiece;
           const uint32_t vslot = sbase + vs * L::kVSlot;
 #pragma unroll
@@ -1077,8 +1100,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               mma_ss(tmem + 256u * nh, adesc, bdesc, kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
             }
           }
-          mma_commit(bar(Ctl::kVtEmpty, vs));
-          mma_commit(bar(Ctl::kPvDone, pb));
+          mma_commit(bar(Ctl::kPvDone, pb));  // frees P buffer pb and V slot vs
           last_bar = bar(Ctl::kPvDone, pb);  // tracks every MMA issued so far
           last_parity = (u / kPBufs) & 1u;
           issued = true;
@@ -1269,6 +1291,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // column h of a P^T piece: M block h / 64, 16-byte chunk (h % 64) / 8
     const uint32_t col_blk = static_cast<uint32_t>(h >> 6) * 4096u + (static_cast<uint32_t>(h) & 7u) * 2u;
     const uint32_t col_chunk = (static_cast<uint32_t>(h) & 63u) >> 3;
+    // byte offset of row r of that column: (r / 8) 1024 + xo[r % 8]
+    uint32_t xo[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xo[k] = col_blk + sw128_off(static_cast<uint32_t>(k), col_chunk);
     float l_acc = 0.f;
     bool ok = true;
     for (int u = 0; u < n_pc; ++u) {
@@ -1295,13 +1321,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bar(Ctl::kOCorr, 0));
       }
-      const uint32_t pcol = sbase + L::kP + pb * kPiece + col_blk;
-      float part = 0.f;
-#pragma unroll 8
+      const uint32_t pbase = sbase + L::kP + pb * kPiece;
+      float part[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
       for (int r = 0; r < kSub; ++r)
-        part += f16_bits_to_f32(
-            static_cast<uint16_t>(ld_shared_u16(pcol + sw128_off(static_cast<uint32_t>(r), col_chunk))));
-      l_acc += part;
+        part[r & 3] += f16_bits_to_f32(static_cast<uint16_t>(
+            ld_shared_u16(pbase + xo[r & 7] + static_cast<uint32_t>(r >> 3) * 1024u)));
+      l_acc += (part[0] + part[1]) + (part[2] + part[3]);
       if (!warp_wait(bar(Ctl::kPvDone, pb), (u / kPBufs) & 1u, abort_addr, lim)) {
         ok = false;
         break;
