@@ -69,7 +69,6 @@ constexpr int kQTiles = 9;                   // Q: 8 latent 64-dim tiles + the r
 // commit) off the tensor pipe's critical path.
 constexpr int kChunksPerTile = 5;
 constexpr int kPBufs = 6;                    // output CTA: P pieces in flight
-constexpr int kVSlots = 3;                   // output CTA: V slots of 32 rows
 // Gather stage u lands in data slot u % stages but completes and is released
 // on barrier pair u % 4. The score CTA's four quadrant warps wait for four
 // consecutive stages at once; with fewer than four data slots, a barrier per
@@ -131,6 +130,11 @@ struct TcLayout {
   static constexpr int kEndS = kAFS + kAFBytes + 3 * kFlagBytes;
   // output CTA
   static constexpr int kVSlot = 32 * 1024;                  // 32 rows x 512 dims FP16 (MN-major)
+  // A V slot is refilled once the P V MMAs of the piece kVSlots back have
+  // completed and the slot has been dequantised again, so the slot count
+  // sets how many pieces the output CTA keeps in flight: four where shared
+  // memory allows (NVFP4), three for the wider FP8 gather stages.
+  static constexpr int kVSlots = kNv ? 4 : 3;
   static constexpr int kP = kVSlots * kVSlot;               // kPBufs P^T pieces
   static constexpr int kRawO = kP + kPBufs * kPiece;
   static constexpr int kAFO = kRawO + kStagesO * kStageO;  // factors + flags per P buffer
@@ -654,7 +658,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       st_shared_u32(ctl + Ctl::kSentCnt + 4 * s, 0u);
       st_shared_u32(ctl + Ctl::kSent + 4 * s, 0u);
     }
-    for (int s = 0; s < kVSlots; ++s) mbar_init(bar(Ctl::kVtFull, s), 8);
+    for (int s = 0; s < L::kVSlots; ++s) mbar_init(bar(Ctl::kVtFull, s), 8);
     for (int s = 0; s < kPBufs; ++s) {
       mbar_init(bar(Ctl::kPFull, s), 1);
       mbar_init(bar(Ctl::kPEmpty, s), 4);
@@ -943,14 +947,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // V slot u % 3 is free once the P V MMAs of piece u - 3 have completed
     // (the one commit per piece, on its P buffer's PvDone barrier)
     auto v_slot_free = [&](int u) {
-      if (u < kVSlots) return true;
-      const int v = u - kVSlots;
+      if (u < L::kVSlots) return true;
+      const int v = u - L::kVSlots;
       return warp_wait(bar(Ctl::kPvDone, v % kPBufs), (v / kPBufs) & 1u, abort_addr, lim);
     };
     for (int u = 0; u < n_pc && run; ++u) {
       const int s = u % L::kStagesO;   // data slot
       const int rb = u % kRawBars;     // barrier pair
-      const int vs = u % kVSlots;
+      const int vs = u % L::kVSlots;
       if (!warp_wait(bar(Ctl::kRawFull, rb), (u / kRawBars) & 1u, abort_addr, lim)) break;
       const uint32_t mask = mask_of(u);
       const uint32_t vslot = sbase + vs * L::kVSlot;
@@ -1074,7 +1078,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool p_ready = false, v_ready = false;
         for (int u = 0; u < n_pc; ++u) {
           const int pb = u % kPBufs;
-          const int vs = u % kVSlots;
+          const int vs = u % L::kVSlots;
           // P (and any rescale of O) first, then the V slot
           if (!p_ready &&
               !wait_bar<true>(bar(Ctl::kPFull, pb), (u / kPBufs) & 1u, abort_addr, lim))
@@ -1084,11 +1088,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!wait_bar(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr, lim)) break;
             ++n_corr;
           }
-          if (!v_ready && !wait_bar(bar(Ctl::kVtFull, vs), (u / kVSlots) & 1u, abort_addr, lim))
+          if (!v_ready && !wait_bar(bar(Ctl::kVtFull, vs), (u / L::kVSlots) & 1u, abort_addr, lim))
             break;
           tc_fence_after();
           p_ready = mbar_ready<true>(bar(Ctl::kPFull, (u + 1) % kPBufs), ((u + 1) / kPBufs) & 1u);
-          v_ready = mbar_ready(bar(Ctl::kVtFull, (u + 1) % kVSlots), ((u + 1) / kVSlots) & 1u);
+          v_ready = mbar_ready(bar(Ctl::kVtFull, (u + 1) % L::kVSlots), ((u + 1) / L::kVSlots) & 1u);
           const uint32_t pbuf = sbase + L::kP + pb * kPiece;
           const uint32_t vslot = sbase + vs * L::kVSlot;
 #pragma unroll
