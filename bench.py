@@ -52,6 +52,10 @@ def parse():
     ap.add_argument("--staged", action="store_true",
                     help="fused decode vs the staged comparison path (selected rows to an FP8 "
                          "buffer, then the FP8 decode) on --config; one JSON line")
+    ap.add_argument("--cpu-table", action="store_true",
+                    help="CPU baseline over every config: the oracle timed single-threaded and "
+                         "on all host threads on a bounded sample, scaled to the full config; "
+                         "one JSON line per config and thread count (no GPU)")
     ap.add_argument("--sweep", action="store_true",
                     help="head sweep (16/32/64/128 heads on decode_batch) and the 15 query "
                          "tokens x 16 heads x top-2048 point; one JSON line per point")
@@ -444,6 +448,79 @@ def oracle_sample(wl, fmt, budget_s, max_tokens=None, heads=None):
     return secs, kv_full, threads, desc
 
 
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (x86 model name, or Arm implementer/part)."""
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+    except OSError:
+        pass
+    if "model name" in fields:
+        return fields["model name"]
+    parts = [f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part", "CPU variant") if k in fields]
+    return ", ".join(parts) or "unknown"
+
+
+def run_cpu_table(args):
+    """The fp64 oracle per config, 1 thread and all threads, on bounded samples.
+
+    A sample is whole query tokens (all heads) until about `budget` seconds
+    have passed; the full-config time is the sample time scaled by the valid
+    rows of all tokens over those of the sample. The append configuration
+    also times the oracle append of its new tokens.
+    """
+    import oracle
+    from workloads import CONFIG_NAMES, make_append_batch, make_queries, make_rows, make_workload
+    from workloads import referenced_tokens
+    nmax = oracle.max_threads()
+    model = cpu_model()
+    for name in CONFIG_NAMES:
+        wl = make_workload(name)
+        fmt = 0
+        rb = ROW_BYTES[fmt]
+        stride = 64 * rb
+        pool = np.zeros(wl.num_blocks * stride, np.uint8)
+        seq, pos = referenced_tokens(wl)
+        lat, rope = make_rows(wl, int(seq.size))
+        oracle.append(lat, rope, seq, pos, wl.block_table, 64, pool, wl.num_blocks, stride, fmt)
+        ql, qr = make_queries(wl)
+        rows_all = int((wl.topk_idx >= 0).sum())
+        for threads in sorted({1, nmax}):
+            budget = 6.0 if threads == 1 else 3.0
+            t0 = time.perf_counter()
+            done = rows = 0
+            for t in range(wl.num_q):
+                oracle.sparse_mla_decode(ql[t:t + 1], qr[t:t + 1], wl.q_seq[t:t + 1],
+                                         wl.topk_idx[t:t + 1], wl.block_table, wl.seq_lens, 64,
+                                         pool, wl.num_blocks, stride, fmt, wl.sm_scale,
+                                         nthreads=threads)
+                done += 1
+                rows += int((wl.topk_idx[t] >= 0).sum())
+                if time.perf_counter() - t0 > budget:
+                    break
+            secs = time.perf_counter() - t0
+            full_s = secs * rows_all / max(rows, 1)
+            line = {"cpu_table": name, "threads": threads, "cpu_model": model,
+                    "host_threads": nmax, "decode_s_full_config": round(full_s, 4),
+                    "decode_us_per_row_head": round(secs / max(rows, 1) / wl.num_heads * 1e6, 4),
+                    "sample": f"{done} of {wl.num_q} query tokens, all {wl.num_heads} heads, "
+                              f"{rows} valid rows, fp64 C oracle, NVFP4 rows",
+                    "config": describe(wl, fmt)}
+            if name == "append_dense" and threads == 1:  # the oracle append is single-threaded
+                aseq, apos, alat, arope = make_append_batch(wl)
+                apool = np.zeros(wl.num_blocks * stride, np.uint8)
+                t1 = time.perf_counter()
+                oracle.append(alat, arope, aseq, apos, wl.block_table, 64, apool, wl.num_blocks,
+                              stride, fmt)
+                line["append_s"] = round(time.perf_counter() - t1, 4)
+                line["append_tokens"] = int(aseq.size)
+            print(json.dumps(line), flush=True)
+
+
 def run_reference(args):
     from workloads import make_workload
     wl = make_workload(args.config)
@@ -784,6 +861,10 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             run_reference(args)
+        return
+    if args.cpu_table:
+        if rank == 0:
+            run_cpu_table(args)
         return
     if args.sweep:
         if rank == 0:

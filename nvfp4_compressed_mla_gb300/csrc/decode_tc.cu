@@ -70,12 +70,12 @@ constexpr int kQTiles = 9;                   // Q: 8 latent 64-dim tiles + the r
 constexpr int kChunksPerTile = 5;
 constexpr int kPBufs = 6;                    // output CTA: P pieces in flight
 // Gather stage u lands in data slot u % stages but completes and is released
-// on barrier pair u % 4. The score CTA's four quadrant warps wait for four
+// on barrier pair u % 8. The score CTA's four quadrant warps wait for four
 // consecutive stages at once; with fewer than four data slots, a barrier per
 // data slot would let a waiter be two phases ahead of it (and a parity wait
-// cannot tell those phases apart). With four pairs every waiter is at most
-// one phase ahead.
-constexpr int kRawBars = 4;
+// cannot tell those phases apart). With at least four pairs, and no fewer
+// than the data slots, every waiter is at most one phase ahead.
+constexpr int kRawBars = 8;
 // Lazy rescale threshold (log2 units): a head's reference maximum moves only
 // when a score exceeds it by more than kTau, so P = 2^(s c - m_ref) <= 2^15,
 // which FP16 holds (largest finite value 65504); l <= 2^15 x top-k stays far
@@ -116,18 +116,25 @@ struct TcLayout {
   static constexpr int kGroupO = (4 * kRowO + 127) / 128 * 128;  // 1152 / 2176
   static constexpr int kStageS = (kSub / 4) * kGroupS;
   static constexpr int kStageO = (kSub / 4) * kGroupO;
-  static constexpr int kStagesS = kNv ? 4 : 2;
+  // P^T pieces reach the output CTA either through a local staging slot and
+  // one bulk copy per piece (NVFP4 rows), or as the softmax warps' own stores
+  // into the peer (FP8 rows: the staging's 32 KB buy the score CTA's ring a
+  // third stage of the wider rows instead; the stores are slower, the deeper
+  // gather prefetch wins for those rows).
+  static constexpr bool kDirectP = !kNv;
+  static constexpr int kStagesS = kNv ? 4 : 3;
   static constexpr int kStagesO = kNv ? 4 : 3;
   // score CTA
   static constexpr int kQTile = 16384;                      // 128 heads x 64 dims (SW128)
   static constexpr int kQ = 0;                              // 9 tiles: 8 latent + rope
   static constexpr int kRawS = kQ + kQTiles * kQTile;
-  static constexpr int kStg = kRawS + kStagesS * kStageS;   // 4 P^T staging slots
-  static constexpr int kNegM = kStg + kPiecesPerTile * kPiece;  // -(reference maximum) per head
+  static constexpr int kStg = kRawS + kStagesS * kStageS;   // 4 P^T staging slots (NVFP4)
+  static constexpr int kNegM = kStg + (kDirectP ? 0 : kPiecesPerTile * kPiece);  // -(ref. maximum)
   static constexpr int kAlpha = kNegM + 512;                // rescale factor per head
   static constexpr int kFlags = kAlpha + 512;               // per softmax warp: "rescaled"
   static constexpr int kAFS = kFlags + 16;                  // factors + flags of slot 0, flags 1-3
-  static constexpr int kEndS = kAFS + kAFBytes + 3 * kFlagBytes;
+  static constexpr int kColMax = kAFS + kAFBytes + 3 * kFlagBytes;  // per softmax warp: column maxima
+  static constexpr int kEndS = kColMax + kPiecesPerTile * 512;
   // output CTA
   static constexpr int kVSlot = 32 * 1024;                  // 32 rows x 512 dims FP16 (MN-major)
   // A V slot is refilled once the P V MMAs of the piece kVSlots back have
@@ -153,12 +160,12 @@ struct TcLayout {
 
 // Control block (barriers and a few words): same offset in both CTAs of the cluster.
 struct Ctl {
-  static constexpr int kRawFull = 0, kRawEmpty = 32, kChunkFull = 192, kChunkEmpty = 264, kSFull = 336, kSEmpty = 352,
+  static constexpr int kRawFull = 0, kRawEmpty = 64, kChunkFull = 192, kChunkEmpty = 264, kSFull = 336, kSEmpty = 352,
                        kSentCnt = 368, kSent = 400, kQFull = 440,
                        kQReady = 448, kVtFull = 456, kPFull = 504, kPEmpty = 552,
                        kPvDone = 600, kOCorr = 648, kStats = 656, kSentBar = 664, kTmem = 672,
-                       kAbort = 676, kLastStage = 688, kMaskRing = 704,
-                       kEnd = 960;
+                       kAbort = 676, kMaskRing = 704, kLastStage = 960,
+                       kEnd = 992;
 };
 static_assert(Ctl::kEnd <= TcLayout<NVFP4_MLA_ROW_NVFP4_352>::kCtlBytes, "control block");
 
@@ -256,11 +263,20 @@ __device__ __forceinline__ void cluster_sync() {
                "barrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
 }
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                              uint32_t d) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b),
+               "r"(c), "r"(d)
+               : "memory");
+}
 __device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void fence_proxy_async_cta() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -286,14 +302,6 @@ __device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
-}
-__device__ __forceinline__ uint64_t ld_shared_u64(uint32_t addr) {
-  uint64_t v;
-  asm volatile("ld.shared.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_shared_u64(uint32_t addr, uint64_t v) {
-  asm volatile("st.shared.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 
 // tcgen05
@@ -660,7 +668,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < L::kVSlots; ++s) mbar_init(bar(Ctl::kVtFull, s), 8);
     for (int s = 0; s < kPBufs; ++s) {
-      mbar_init(bar(Ctl::kPFull, s), 1);
+      // the bulk copy's arrive + bytes, or each lane of the sending warp
+      mbar_init(bar(Ctl::kPFull, s), L::kDirectP ? 32 : 1);
       mbar_init(bar(Ctl::kPEmpty, s), 4);
       mbar_init(bar(Ctl::kPvDone, s), 1);
     }
@@ -1126,13 +1135,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const float c = p.score_scale;
     const uint64_t c2 = f32x2(c, c);
     const int hchunks = (p.num_heads + 31) >> 5;  // head chunks with live heads
-    const uint32_t stg = sbase + L::kStg + q4 * kPiece;
+    const uint32_t stg = sbase + L::kStg + q4 * kPiece;  // NVFP4 rows
+    const uint32_t colmax = sbase + L::kColMax + q4 * 512;
     const uint32_t peer_p = map_rank(sbase + L::kP, peer);
     const uint32_t peer_af = map_rank(sbase + L::kAFO, peer);
     const uint32_t peer_ctl = map_rank(ctl, peer);
     // P^T of this warp's 32 rows for head chunk hc (32 heads) from S^T at
-    // column `scol`; returns the largest exponent t = s c - m_ref of a live row.
-    auto p_chunk = [&](uint32_t scol, int hc, bool live) -> float {
+    // column `scol`, stored at `dst` (the staging slot, or the peer's P
+    // buffer); returns the largest exponent t = s c - m_ref of a live row.
+    auto p_chunk = [&](uint32_t scol, int hc, bool live, uint32_t dst) -> float {
       uint32_t sv[32];
       tmem_ld32(tmem + lane_base + scol + 32u * hc, sv);
       float nm[32];
@@ -1157,11 +1168,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         pk[q] = live ? pack_f16x2(ex2(t0), ex2(t1)) : 0u;
       }
       // heads 32 hc .. + 31 = M block hc / 2, 16-byte chunks 4 (hc % 2) .. + 3
-      const uint32_t blk = stg + static_cast<uint32_t>(hc >> 1) * 4096u;
+      const uint32_t blk = dst + static_cast<uint32_t>(hc >> 1) * 4096u;
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc)
-        st_shared_v4(blk + sw128_off(static_cast<uint32_t>(lane), 4 * (hc & 1) + cc), pk[4 * cc],
-                     pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      for (int cc = 0; cc < 4; ++cc) {
+        const uint32_t a = blk + sw128_off(static_cast<uint32_t>(lane), 4 * (hc & 1) + cc);
+        if constexpr (L::kDirectP)
+          st_cluster_v4(a, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        else
+          st_shared_v4(a, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+      }
       return live ? tmx : -INFINITY;
     };
     for (int i = 0; i < n_tiles && ok; ++i) {
@@ -1172,9 +1187,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int u = kPiecesPerTile * i + q4;
       const bool live = (mask_of(u) >> lane) & 1u;
-      // this warp's staging slot: its copy of the previous tile has read it
-      if (lane == 0) bulk_wait_read<0>();
-      __syncwarp();
+      const int pb = u % kPBufs;
+      uint32_t dst = stg;
+      if constexpr (L::kDirectP) {
+        // piece u is written straight into the peer's P buffer u % 6, once the
+        // peer has released it
+        uint32_t free_ok = 1u;
+        if (lane == 0)
+          free_ok = wait_bar<true>(bar(Ctl::kPEmpty, pb), ((u / kPBufs) & 1u) ^ 1u, abort_addr, lim)
+                        ? 1u : 0u;
+        ok = __shfl_sync(0xffffffffu, free_ok, 0) != 0u;
+        if (!ok) break;
+        dst = peer_p + static_cast<uint32_t>(pb) * kPiece;
+      } else {
+        // this warp's staging slot: its copy of the previous tile has read it
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
       // Pass 0 computes P against the current references. A live score above
       // its head's reference by more than tau (every first live score
       // included) moves the reference to the tile's maximum: all four warps
@@ -1185,12 +1214,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int pass = 0; pass < 2; ++pass) {
         float tmx = -INFINITY;
 #pragma unroll 1
-        for (int hc = 0; hc < hchunks; ++hc) tmx = fmaxf(tmx, p_chunk(scol, hc, live));
+        for (int hc = 0; hc < hchunks; ++hc) tmx = fmaxf(tmx, p_chunk(scol, hc, live, dst));
         if (pass == 1) break;
         exceed = group_or(tmx > kTau);
         if (!exceed) break;
-        // column maxima of this warp's live rows (parked in its staging slot,
-        // which pass 1 overwrites), then per head over the four warps
+        // column maxima of this warp's live rows, then per head over the four warps
 #pragma unroll 1
         for (int hc = 0; hc < 4; ++hc) {
           uint32_t sv[32];
@@ -1199,7 +1227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float v[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = live ? __uint_as_float(sv[j]) : -INFINITY;
-          st_shared_u32(stg + 4 * (32 * hc + lane), __float_as_uint(warp_colmax(v, lane)));
+          st_shared_u32(colmax + 4 * (32 * hc + lane), __float_as_uint(warp_colmax(v, lane)));
         }
         group_sync();
         {
@@ -1207,7 +1235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           float mx = -INFINITY;
 #pragma unroll
           for (int w = 0; w < 4; ++w)
-            mx = fmaxf(mx, __uint_as_float(ld_shared_u32(sbase + L::kStg + w * kPiece + 4 * h)));
+            mx = fmaxf(mx, __uint_as_float(ld_shared_u32(sbase + L::kColMax + w * 512 + 4 * h)));
           const float mxs = mx * c;
           const float m_old = -__uint_as_float(ld_shared_u32(sbase + L::kNegM + 4 * h));
           float alpha = 1.f;
@@ -1229,6 +1257,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Ctl::kSEmpty, s2));
+      if constexpr (L::kDirectP) {
+        // factors (tile's first piece) or zero flags straight into the peer's
+        // factor block; every lane releases its stores and arrives
+        const uint32_t af = peer_af + static_cast<uint32_t>(pb) * kAFBytes;
+        if (q4 == 0) {
+          if (exceed) {
+            const uint4 a = ld_shared_v4(sbase + L::kAlpha + 16 * lane);
+            st_cluster_v4(af + 16 * lane, a.x, a.y, a.z, a.w);
+          }
+          if (lane == 0) {
+            const uint4 f = exceed ? ld_shared_v4(sbase + L::kFlags) : make_uint4(0u, 0u, 0u, 0u);
+            st_cluster_v4(af + 512, f.x, f.y, f.z, f.w);
+          }
+        } else if (lane == 0) {
+          st_cluster_v4(af + 512, 0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_cluster();  // the peer's MMAs read P through the async proxy
+        mbar_arrive_cluster(peer_ctl + Ctl::kPFull + 8 * pb);
+        continue;
+      }
       // rescale factors travel with the tile's first piece (slot 0); pieces
       // 1-3 carry zero flags
       if (q4 == 0) {
@@ -1249,7 +1297,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // it, with the rescale factors (tile's first piece) or zero flags.
       uint32_t sent_ok = 1u;
       if (lane == 0) {
-        const int pb = u % kPBufs;
         sent_ok = wait_bar<true>(bar(Ctl::kPEmpty, pb), ((u / kPBufs) & 1u) ^ 1u, abort_addr, lim)
                       ? 1u : 0u;
         if (sent_ok) {
@@ -1271,7 +1318,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     ok = group_and(ok);
     // the peer learns how many pieces went into each P buffer (it drains them
     // on abort), then the final reference maximum of head h = tid
-    if (tid == 0) {
+    if (tid == 0 && !L::kDirectP) {
 #pragma unroll
       for (int pb = 0; pb < kPBufs; ++pb)
         st_cluster_u32(peer_ctl + Ctl::kSent + 4 * pb, ld_shared_u32(ctl + Ctl::kSentCnt + 4 * pb));
@@ -1458,7 +1505,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lu > 0) drain_bar(bar(Ctl::kRawFull, s), ((lu - 1) / kRawBars) & 1u);
     }
     if (rank == 0) drain_bar(bar(Ctl::kQFull, 0), 0);
-    if (rank == 1) {
+    if (rank == 1 && !L::kDirectP) {  // P copies (stored P is ordered by the cluster barrier)
       drain_bar<true>(bar(Ctl::kSentBar, 0), 0);
       for (int pb = 0; pb < kPBufs; ++pb) {  // pieces go into a buffer in order
         const uint32_t c = ld_shared_u32(ctl + Ctl::kSent + 4 * pb);
