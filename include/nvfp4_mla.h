@@ -113,8 +113,10 @@ int32_t nvfp4_mla_append(const void* latent, const void* rope, const int32_t* se
  * Number of top-k splits sparse_mla_decode uses for this shape when its
  * `num_splits` argument is 0 (batch-adaptive, after the post's "adjust the
  * cluster to the batch" change in section "Native NVFP4 sparse MLA decode
- * kernel"). Depends on the SM count of the current device. Returns >= 1,
- * or 0 when the shape is invalid or the device query fails.
+ * kernel"). Depends on the SM count of the current device. A split covers
+ * at least two 128-slot tiles, and a top-k of fewer than four tiles is not
+ * split. Returns >= 1, or 0 when the shape is invalid or the device query
+ * fails.
  */
 int32_t sparse_mla_decode_num_splits(int32_t num_q, int32_t num_heads, int32_t topk);
 

@@ -70,13 +70,16 @@ __global__ void __launch_bounds__(128) combine_kernel(const Params p) {
 }
 
 // Splits per query token: enough (token, split) clusters to fill the GPU
-// once (two SMs per cluster), never more splits than 64-slot tiles.
+// once (two SMs per cluster), with at least two 128-slot tiles per split and
+// no split below four tiles: a split saves its share of the tiles but costs
+// the combine launch and the workspace round trip, about two tiles' time.
 int auto_splits(int num_q, int num_heads, int topk, int sms) {
   (void)num_heads;
   const int tiles = (topk + kTile - 1) / kTile;
+  if (tiles < 4) return 1;
   const int clusters = sms / 2;
   int s = num_q >= clusters ? 1 : clusters / num_q;
-  s = min(s, min(tiles, 64));
+  s = min(s, min(tiles / 2, 64));
   return max(s, 1);
 }
 

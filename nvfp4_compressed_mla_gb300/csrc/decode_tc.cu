@@ -14,7 +14,7 @@
 // contractions of the absorbed-MLA step its own SM:
 //
 //   rank 0, "score" CTA: S^T = K Q^T per 128-row tile (M = 128 rows,
-//     N = 128 heads, K = 576). The dequant warps expand the gathered rows
+//     N = the heads rounded up to 32, K = 576). The dequant warps expand the gathered rows
 //     (thread = row) straight into tensor memory, where they are the MMA's A
 //     operand: a ring of 64-dimension chunks, so the FP16 K tile never
 //     touches shared memory. Q (FP16, all 576 dimensions of the 128 heads)
@@ -85,7 +85,17 @@ constexpr float kTau = 15.0f;
 constexpr long long kDrainCycles = 1ll << 31;
 // tcgen05 instruction descriptors (kind::f16, FP16 A/B, FP32 D):
 //   bit 4 D = f32, bit 15 A MN-major, bit 16 B MN-major, N >> 3 at 17, M >> 4 at 24
-constexpr uint32_t kIdescQK = (1u << 4) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+// QK: N = the live heads rounded up to 32 (the softmax reads 32-column head chunks)
+__host__ __device__ constexpr int qk_n(int num_heads) {
+  return num_heads >= 128 ? 128 : (num_heads + 31) / 32 * 32;
+}
+// Q rows copied per tile: the live heads rounded up to 8 (rows past them are zeroed)
+__host__ __device__ constexpr int q_rows(int num_heads) {
+  return num_heads >= 128 ? 128 : (num_heads + 7) / 8 * 8;
+}
+__device__ __forceinline__ uint32_t idesc_qk(int num_heads) {
+  return (1u << 4) | ((static_cast<uint32_t>(qk_n(num_heads)) >> 3) << 17) | ((128u >> 4) << 24);
+}
 constexpr uint32_t kIdescPV =
     (1u << 4) | (1u << 15) | (1u << 16) | ((256u >> 3) << 17) | ((128u >> 4) << 24);
 constexpr uint32_t kAFBytes = 528;           // rescale factors of 128 heads + 4 flag words
@@ -689,12 +699,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t tmem = ld_shared_u32(ctl + Ctl::kTmem);
   if (tmem != 0u && tid == 0) st_shared_u32(abort_addr, 1u);  // MMA operands assume base 0
 
-  // Score CTA: Q of this token (bf16, the 128 rows from row t * H; rows of
-  // other tokens or past the end are zeroed at conversion) by nine 2-D tensor
-  // copies into 128-byte-swizzled tiles, the layout of the MMA's B operand.
+  // Score CTA: Q of this token (bf16, the rows from row t * H: the live heads
+  // rounded up to 8; rows of other tokens, past the end or past the copied
+  // ones are zeroed at conversion) by nine 2-D tensor copies into
+  // 128-byte-swizzled tiles, the layout of the MMA's B operand.
   if (rank == 0 && tid == 32) {
     const uint32_t qbar = bar(Ctl::kQFull, 0);
-    mbar_arrive_tx(qbar, static_cast<uint32_t>(kQTiles * L::kQTile));
+    mbar_arrive_tx(qbar, static_cast<uint32_t>(kQTiles * 128 * q_rows(p.num_heads)));
     const int32_t y = t * p.num_heads;
     for (int kb = 0; kb < 8; ++kb)
       tma_load_2d(sbase + L::kQ + kb * L::kQTile, &tm_ql, 64 * kb, y, qbar);
@@ -1041,6 +1052,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           // columns starts at TMEM address 0 (checked at set-up); a
           // descriptor's address field counts 16 bytes.
           const uint64_t qd = sw128_desc(sbase + L::kQ);
+          const uint32_t idesc = idesc_qk(p.num_heads);
           bool run = true;
           // Whether chunk q is known to be in the ring: the next chunk's
           // barrier is tested (without blocking) before this chunk's MMAs go
@@ -1071,7 +1083,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (kk < nk)
                   mma_ts(dcol, a + 8u * kk,
                          bd + static_cast<uint64_t>((kk >> 2) * (L::kQTile >> 4) + 2 * (kk & 3)),
-                         kIdescQK, (kb | kk) != 0 ? 1u : 0u);
+                         idesc, (kb | kk) != 0 ? 1u : 0u);
               mma_commit(bar(Ctl::kChunkEmpty, cs));
               last_bar = bar(Ctl::kChunkEmpty, cs);
               last_parity = (q / L::kKSlots) & 1u;
@@ -1591,12 +1603,13 @@ bool row_maps(const DecodeParams& p, CUtensorMap* ms, CUtensorMap* mo) {
 }
 
 // q_latent [num_q * H, 512] and q_rope [num_q * H, 64] bf16 as 2-D tensors
-// with 128-row x 64-column boxes in the 128-byte swizzle the MMA reads.
+// with (heads rounded up to 8)-row x 64-column boxes in the 128-byte swizzle
+// the MMA reads.
 bool q_maps(const DecodeParams& p, CUtensorMap* ml, CUtensorMap* mr) {
   EncodeTiledFn enc = encode_tiled();
   const int64_t rows = static_cast<int64_t>(p.num_q) * p.num_heads;
   if (enc == nullptr || rows <= 0 || rows > 0x7FFFFFFFll) return false;
-  const cuuint32_t box[2] = {64, 128};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(q_rows(p.num_heads))};
   const cuuint32_t es[2] = {1, 1};
   const cuuint64_t dl[2] = {static_cast<cuuint64_t>(kLatent), static_cast<cuuint64_t>(rows)};
   const cuuint64_t sl[1] = {static_cast<cuuint64_t>(kLatent * 2)};
