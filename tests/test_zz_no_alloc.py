@@ -57,7 +57,7 @@ def test_noalloc_matches_workspace_entry_two_calls_in_a_row():
     lib = _native.load()
     cases = [
         (build_case(make_workload("agent", num_seqs=3, seq_len=6000, topk=1000, num_heads=32)), 4),
-        (build_case(make_workload("tiny", num_seqs=2, seq_len=900, topk=300, q_per_seq=3),
+        (build_case(make_workload("tiny", num_seqs=2, seq_len=900, topk=600, q_per_seq=3),
                     row_format=1, latent_scale=0.5, rope_scale=2.0), 0),
     ]
     for case, splits in cases:  # two calls in a row, different shapes and formats
