@@ -156,7 +156,9 @@ struct TcLayout {
   static constexpr int kRawO = kP + kPBufs * kPiece;
   static constexpr int kAFO = kRawO + kStagesO * kStageO;  // factors + flags per P buffer
   static constexpr int kFinO = kAFO + kPBufs * kAFBytes;    // final reference maximum per head
-  static constexpr int kEndO = kFinO + 512;
+  static constexpr int kScO = kFinO + 512;                  // output scale per head (epilogue)
+  static constexpr int kEpiOk = kScO + 512;                 // the unit's outputs are valid
+  static constexpr int kEndO = kEpiOk + 16;
   static constexpr int kCtl = ((kEndS > kEndO ? kEndS : kEndO) + 15) / 16 * 16;
   static constexpr int kCtlBytes = 1056;
   static constexpr int kBytes = kCtl + kCtlBytes;
@@ -438,6 +440,8 @@ __device__ __forceinline__ bool group_and(bool v) {
   return r != 0;
 }
 __device__ __forceinline__ void group_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier 2 over the output CTA's epilogue warps: 0-3 and 8-15 (384 threads).
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 384;" ::: "memory"); }
 
 // four rows (y0..y3) of a 2-D tensor map, one box each, into consecutive boxes at dst
 __device__ __forceinline__ void gather4(uint32_t dst, const CUtensorMap* tm, int32_t y0, int32_t y1,
@@ -721,6 +725,72 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   };
   auto mask_of = [&](int u) {  // live-row mask of stage u (published by its gather warp)
     return *reinterpret_cast<volatile uint32_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31));
+  };
+  // Output CTA epilogue, shared by the four correction warps and the eight V
+  // dequant warps (idle by then): warp (quadrant q, part) reads columns chunk
+  // cc = part, part + 3, ... of its quadrant's 32 heads from TMEM, scales them
+  // by the head's factor and stages them in the head's row in shared memory
+  // (over the V slots and P buffers, which every reader has finished with at
+  // the first barrier); then warp e of 12 writes rows e, e + 12, ... with
+  // stores that are contiguous across the warp. fp32 rows (fp32 output,
+  // split-K partials) go in two halves of 256 columns. Every warp passes the
+  // same barriers: the first one always, then two per half when the unit's
+  // outputs are valid.
+  auto epilogue = [&](int q, int part, int e) {
+    epi_sync();  // the factors and the valid flag are published; every P / V reader is done
+    if (ld_shared_u32(sbase + L::kEpiOk) == 0u) return;
+    tc_fence_after();
+    constexpr uint32_t kOutPitch = 1024 + 16;
+    const int h = 32 * q + lane;
+    const float sc = __uint_as_float(ld_shared_u32(sbase + L::kScO + 4 * h));
+    const uint32_t lq = static_cast<uint32_t>(32 * q) << 16;
+    const bool single = p.num_splits == 1;
+    const bool f32 = !(single && !p.out_fp32);
+    const int H = p.num_heads;
+    const uint32_t stg = sbase + static_cast<uint32_t>(h) * kOutPitch;
+#pragma unroll 1
+    for (int hv = 0; hv < (f32 ? 2 : 1); ++hv) {
+#pragma unroll 1
+      for (int cc = part; cc < (f32 ? 8 : 16); cc += 3) {
+        uint32_t r[32];
+        tmem_ld32(tmem + lq + 256u * hv + 32u * cc, r);
+        tmem_ld_wait();
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * sc;
+        if (!f32) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            st_shared_v4(stg + cc * 64 + k * 16, pack_bf16x2(v[8 * k], v[8 * k + 1]),
+                         pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                         pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                         pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            st_shared_v4(stg + cc * 128 + k * 16, __float_as_uint(v[4 * k]),
+                         __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                         __float_as_uint(v[4 * k + 3]));
+        }
+      }
+      epi_sync();  // every row staged
+      // rows of 1 KB (a bf16 row or an fp32 half row)
+#pragma unroll 1
+      for (int hh = e; hh < H; hh += 12) {
+        const int64_t qhh = static_cast<int64_t>(t) * H + hh;
+        const int64_t phh = (static_cast<int64_t>(t) * p.num_splits + split) * H + hh;
+        uint8_t* dst =
+            !f32 ? reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) + qhh * kLatent)
+            : single
+                ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) + qhh * kLatent + 256 * hv)
+                : reinterpret_cast<uint8_t*>(p.ws + phh * kLatent + 256 * hv);
+        const uint32_t src = sbase + static_cast<uint32_t>(hh) * kOutPitch;
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) = ld_shared_v4(src + k * 512 + lane * 16);
+      }
+      epi_sync();  // every row written: the next half may overwrite the staging
+    }
   };
   // Score CTA: converter g (0..415) turns its share of Q (bf16, as loaded)
   // into FP16 in place, scales folded in, heads >= H zeroed: 16-byte item i =
@@ -1041,6 +1111,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mbar_arrive(bar(Ctl::kRawEmpty, rb));  // stage u read: the gather warp may refill slot s
       }
     }
+    epilogue(warp & 3, 1 + ((warp - kDequantWarp0) >> 2), 4 + (warp - kDequantWarp0));
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issue (one thread)
     if (lane == 0) {
@@ -1408,91 +1479,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     } else {
       ok = false;
     }
-    tc_fence_after();
+    ok = group_and(ok);  // the four correction warps agree
     {
-      const bool live = h < p.num_heads;  // TMEM loads are warp-wide; only stores are per lane
+      const bool live = h < p.num_heads;
       const float inv = !ok ? NAN : (l_fin > 0.f ? 1.f / l_fin : 0.f);
       const float lse_nat = !ok ? NAN : (l_fin > 0.f ? (m_fin + lg2(l_fin)) * kLn2 : -INFINITY);
       const int64_t qh = static_cast<int64_t>(t) * p.num_heads + h;
       const bool single = p.num_splits == 1;
-      const float sc = single ? inv * p.out_mult : inv;
       const int64_t part = (static_cast<int64_t>(t) * p.num_splits + split) * p.num_heads + h;
       const bool f32 = !(single && !p.out_fp32);
-      const int H = p.num_heads;
-      if (!ok) {
+      st_shared_u32(sbase + L::kScO + 4 * h, __float_as_uint(single ? inv * p.out_mult : inv));
+      if (tid == 0) st_shared_u32(sbase + L::kEpiOk, ok ? 1u : 0u);
+      if (!ok && live) {
         // a failed unit: NaN straight to global memory (its shared memory may
         // still receive copies, drained at teardown)
-        if (live) {
 #pragma unroll 1
-          for (int d = 0; d < kLatent; d += 4) {
-            if (!f32)
-              *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + qh * kLatent + d) =
-                  make_uint2(pack_bf16x2(NAN, NAN), pack_bf16x2(NAN, NAN));
-            else if (single)
-              *reinterpret_cast<float4*>(static_cast<float*>(p.out) + qh * kLatent + d) =
-                  make_float4(NAN, NAN, NAN, NAN);
-            else
-              *reinterpret_cast<float4*>(p.ws + part * kLatent + d) =
-                  make_float4(NAN, NAN, NAN, NAN);
-          }
-        }
-      } else {
-        // Rows leave through shared memory over the V slots and P buffers,
-        // once all four correction warps have finished reading the P buffers:
-        // each thread stages its head's row at a padded pitch
-        // (conflict-free), then each warp writes its 32 rows with stores that
-        // are contiguous across the warp. fp32 rows (fp32 output, split-K
-        // partials) go in two halves of 256 columns.
-        constexpr uint32_t kOutPitch = 1024 + 16;
-        const uint32_t stg = sbase + static_cast<uint32_t>(h) * kOutPitch;
-        group_sync();
-#pragma unroll 1
-        for (int hv = 0; hv < (f32 ? 2 : 1); ++hv) {
-#pragma unroll 1
-          for (int cc = 0; cc < (f32 ? 8 : 16); ++cc) {
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_base + 256u * hv + 32u * cc, r);
-            tmem_ld_wait();
-            float v[32];
-#pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = __uint_as_float(r[q]) * sc;
-            if (!f32) {
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                st_shared_v4(stg + cc * 64 + q * 16, pack_bf16x2(v[8 * q], v[8 * q + 1]),
-                             pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                             pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                             pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
-            } else {
-#pragma unroll
-              for (int q = 0; q < 8; ++q)
-                st_shared_v4(stg + cc * 128 + q * 16, __float_as_uint(v[4 * q]),
-                             __float_as_uint(v[4 * q + 1]), __float_as_uint(v[4 * q + 2]),
-                             __float_as_uint(v[4 * q + 3]));
-            }
-          }
-          __syncwarp();
-          // the warp's rows, 1 KB each (a bf16 row or an fp32 half row)
-#pragma unroll 1
-          for (int rr = 0; rr < 32; ++rr) {
-            const int hh = warp * 32 + rr;
-            if (hh >= H) break;
-            const int64_t qhh = static_cast<int64_t>(t) * H + hh;
-            const int64_t phh = (static_cast<int64_t>(t) * p.num_splits + split) * H + hh;
-            uint8_t* dst =
-                !f32 ? reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) + qhh * kLatent)
-                : single
-                    ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) + qhh * kLatent + 256 * hv)
-                    : reinterpret_cast<uint8_t*>(p.ws + phh * kLatent + 256 * hv);
-            const uint32_t src = sbase + static_cast<uint32_t>(hh) * kOutPitch;
-#pragma unroll
-            for (int k = 0; k < 2; ++k)
-              *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) =
-                  ld_shared_v4(src + k * 512 + lane * 16);
-          }
-          __syncwarp();  // the next half overwrites this warp's staging rows
+        for (int d = 0; d < kLatent; d += 4) {
+          if (!f32)
+            *reinterpret_cast<uint2*>(static_cast<uint16_t*>(p.out) + qh * kLatent + d) =
+                make_uint2(pack_bf16x2(NAN, NAN), pack_bf16x2(NAN, NAN));
+          else if (single)
+            *reinterpret_cast<float4*>(static_cast<float*>(p.out) + qh * kLatent + d) =
+                make_float4(NAN, NAN, NAN, NAN);
+          else
+            *reinterpret_cast<float4*>(p.ws + part * kLatent + d) =
+                make_float4(NAN, NAN, NAN, NAN);
         }
       }
+      epilogue(warp, 0, warp);
       if (live) {
         if (single) {
           if (p.lse != nullptr) p.lse[qh] = lse_nat;
