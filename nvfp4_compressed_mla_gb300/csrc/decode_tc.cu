@@ -513,9 +513,34 @@ __device__ __forceinline__ bool mbar_wait_suspend(uint32_t bar, uint32_t parity,
 // Waits for the phase of `bar` with `parity`; false when `limit` clock
 // cycles pass first (the abort flag is then set) or another thread of the
 // CTA has aborted.
+//
+// The test that finds the phase complete is inlined; the waiting loop is one
+// out-of-line copy per scope. The kernel's roles run side by side from
+// different parts of a large body of code, so every copy of a cold path
+// inlined into a hot loop costs instruction-cache space that the loops need.
+template <bool kCluster>
+__device__ __noinline__ bool wait_bar_slow(uint32_t bar, uint32_t parity, uint32_t abort_addr,
+                                           long long limit) {
+  const long long t0 = clock64();
+  const uint32_t hint = suspend_ns(limit);
+  while (true) {
+    if (mbar_wait_suspend<kCluster>(bar, parity, hint)) return true;
+    if (ld_shared_u32(abort_addr) != 0) return false;
+    if (clock64() - t0 > limit) {
+      st_shared_u32(abort_addr, 1u);
+      return false;
+    }
+  }
+}
 template <bool kCluster = false>
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, uint32_t abort_addr,
                                          long long limit) {
+  return mbar_test<kCluster>(bar, parity) || wait_bar_slow<kCluster>(bar, parity, abort_addr, limit);
+}
+// The same wait with its loop inlined, for the MMA thread's critical path.
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_bar_hot(uint32_t bar, uint32_t parity, uint32_t abort_addr,
+                                             long long limit) {
   if (mbar_test<kCluster>(bar, parity)) return true;
   const long long t0 = clock64();
   const uint32_t hint = suspend_ns(limit);
@@ -615,6 +640,150 @@ __device__ __forceinline__ float warp_colmax(float (&v)[32], int lane) {
     }
   }
   return v[0];
+}
+
+// Output CTA epilogue, shared by the four correction warps and the eight V
+// dequant warps (idle by then): warp (quadrant q, part) reads columns chunk
+// cc = part, part + 3, ... of its quadrant's 32 heads from TMEM, scales them
+// by the head's factor and stages them in the head's row in shared memory
+// (over the V slots and P buffers, which every reader has finished with at
+// the first barrier); then warp e of 12 writes rows e, e + 12, ... with
+// stores that are contiguous across the warp. fp32 rows (fp32 output,
+// split-K partials) go in two halves of 256 columns. Every warp passes the
+// same barriers: the first one always, then two per half when the unit's
+// outputs are valid.
+// One out-of-line copy serves both callers (instruction-cache space).
+template <class L>
+__device__ __noinline__ void epilogue_rows(uint32_t sbase, uint32_t tmem, int q, int part, int e,
+                                           int t, int split, int num_heads, int num_splits,
+                                           int out_fp32, void* out, float* ws) {
+  const int lane = threadIdx.x & 31;
+  epi_sync();  // the factors and the valid flag are published; every P / V reader is done
+  if (ld_shared_u32(sbase + L::kEpiOk) == 0u) return;
+  tc_fence_after();
+  constexpr uint32_t kOutPitch = 1024 + 16;
+  const int h = 32 * q + lane;
+  const float sc = __uint_as_float(ld_shared_u32(sbase + L::kScO + 4 * h));
+  const uint32_t lq = static_cast<uint32_t>(32 * q) << 16;
+  const bool single = num_splits == 1;
+  const bool f32 = !(single && !out_fp32);
+  const int H = num_heads;
+  const uint32_t stg = sbase + static_cast<uint32_t>(h) * kOutPitch;
+#pragma unroll 1
+  for (int hv = 0; hv < (f32 ? 2 : 1); ++hv) {
+#pragma unroll 1
+    for (int cc = part; cc < (f32 ? 8 : 16); cc += 3) {
+      uint32_t r[32];
+      tmem_ld32(tmem + lq + 256u * hv + 32u * cc, r);
+      tmem_ld_wait();
+      float v[32];
+#pragma unroll
+      for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * sc;
+      if (!f32) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          st_shared_v4(stg + cc * 64 + k * 16, pack_bf16x2(v[8 * k], v[8 * k + 1]),
+                       pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
+                       pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
+                       pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          st_shared_v4(stg + cc * 128 + k * 16, __float_as_uint(v[4 * k]),
+                       __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
+                       __float_as_uint(v[4 * k + 3]));
+      }
+    }
+    epi_sync();  // every row staged
+    // rows of 1 KB (a bf16 row or an fp32 half row)
+#pragma unroll 1
+    for (int hh = e; hh < H; hh += 12) {
+      const int64_t qhh = static_cast<int64_t>(t) * H + hh;
+      const int64_t phh = (static_cast<int64_t>(t) * num_splits + split) * H + hh;
+      uint8_t* dst =
+          !f32 ? reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(out) + qhh * kLatent)
+          : single
+              ? reinterpret_cast<uint8_t*>(static_cast<float*>(out) + qhh * kLatent + 256 * hv)
+              : reinterpret_cast<uint8_t*>(ws + phh * kLatent + 256 * hv);
+      const uint32_t src = sbase + static_cast<uint32_t>(hh) * kOutPitch;
+#pragma unroll
+      for (int k = 0; k < 2; ++k)
+        *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) = ld_shared_v4(src + k * 512 + lane * 16);
+    }
+    epi_sync();  // every row written: the next half may overwrite the staging
+  }
+}
+
+// Score CTA: converter g (0..415) turns its share of Q (bf16, as loaded)
+// into FP16 in place, scales folded in, heads >= H zeroed: 16-byte item i =
+// g + 416 k is chunk i % 8 of head (i / 8) % 128 of tile i / 1024 (a quarter
+// warp covers one 128-byte row: no bank conflicts). Then the warp signals
+// QReady. A warp whose wait for the Q copies failed converts nothing. One
+// out-of-line copy serves the three roles that convert.
+template <class L>
+__device__ __noinline__ void convert_q_share(uint32_t sbase, uint32_t ctl, int g, int num_heads,
+                                             float lat_mult, float rope_mult, uint32_t abort_addr,
+                                             long long lim) {
+  const bool qok = warp_wait(ctl + Ctl::kQFull, 0, abort_addr, lim);
+  if (qok) {
+    constexpr int kItems = kQTiles * 128 * 8;
+#pragma unroll 1
+    for (int i = g; i < kItems; i += 32 * kQConverters) {
+      const int kb = i >> 10, h = (i >> 3) & 127, c = i & 7;
+      const float m = kb < 8 ? lat_mult : rope_mult;
+      const uint32_t a = sbase + L::kQ + kb * L::kQTile +
+                         sw128_off(static_cast<uint32_t>(h), static_cast<uint32_t>(c));
+      const uint4 x = h < num_heads ? bf16x8_to_f16x8(ld_shared_v4(a), m)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+      st_shared_v4(a, x.x, x.y, x.z, x.w);
+    }
+  }
+  fence_proxy_async_cta();  // generic stores -> visible to the MMA's operand reads
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(ctl + Ctl::kQReady);
+}
+
+// Score CTA softmax warps (thread tid = head h), the rare path of a tile:
+// column maxima of each warp's live rows of S^T (TMEM columns from `scol_addr`,
+// this warp's lanes), then per head over the four warps; a head whose scaled
+// maximum exceeds its reference by more than tau moves its reference there,
+// with the factor alpha that rescales what was accumulated against the old
+// one (0 when there was none). Per warp, a flag says whether any of its heads
+// moved after the unit's first tile. Out of line: it runs on a unit's first
+// tile and rarely after, and stays out of the hot loop's instruction space.
+template <class L>
+__device__ __noinline__ void softmax_new_refs(uint32_t sbase, uint32_t scol_addr, bool live, float c,
+                                              bool not_first) {
+  const int tid = threadIdx.x, lane = tid & 31, q4 = tid >> 5;
+  const uint32_t colmax = sbase + L::kColMax + q4 * 512;
+#pragma unroll 1
+  for (int hc = 0; hc < 4; ++hc) {
+    uint32_t sv[32];
+    tmem_ld32(scol_addr + 32u * hc, sv);
+    tmem_ld_wait();
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = live ? __uint_as_float(sv[j]) : -INFINITY;
+    st_shared_u32(colmax + 4 * (32 * hc + lane), __float_as_uint(warp_colmax(v, lane)));
+  }
+  group_sync();
+  const int h = tid;
+  float mx = -INFINITY;
+#pragma unroll
+  for (int w = 0; w < 4; ++w)
+    mx = fmaxf(mx, __uint_as_float(ld_shared_u32(sbase + L::kColMax + w * 512 + 4 * h)));
+  const float mxs = mx * c;
+  const float m_old = -__uint_as_float(ld_shared_u32(sbase + L::kNegM + 4 * h));
+  float alpha = 1.f;
+  bool resc = false;
+  if (mxs > m_old + kTau) {  // also the first live score (m_old = -inf)
+    alpha = m_old == -INFINITY ? 0.f : ex2(m_old - mxs);
+    st_shared_u32(sbase + L::kNegM + 4 * h, __float_as_uint(-mxs));
+    resc = true;
+  }
+  st_shared_u32(sbase + L::kAlpha + 4 * h, __float_as_uint(alpha));
+  const bool wr = __any_sync(0xffffffffu, resc) && not_first;
+  if (lane == 0) st_shared_u32(sbase + L::kFlags + 4 * q4, wr ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ kernel
@@ -726,95 +895,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   auto mask_of = [&](int u) {  // live-row mask of stage u (published by its gather warp)
     return *reinterpret_cast<volatile uint32_t*>(smem + L::kCtl + Ctl::kMaskRing + 8 * (u & 31));
   };
-  // Output CTA epilogue, shared by the four correction warps and the eight V
-  // dequant warps (idle by then): warp (quadrant q, part) reads columns chunk
-  // cc = part, part + 3, ... of its quadrant's 32 heads from TMEM, scales them
-  // by the head's factor and stages them in the head's row in shared memory
-  // (over the V slots and P buffers, which every reader has finished with at
-  // the first barrier); then warp e of 12 writes rows e, e + 12, ... with
-  // stores that are contiguous across the warp. fp32 rows (fp32 output,
-  // split-K partials) go in two halves of 256 columns. Every warp passes the
-  // same barriers: the first one always, then two per half when the unit's
-  // outputs are valid.
   auto epilogue = [&](int q, int part, int e) {
-    epi_sync();  // the factors and the valid flag are published; every P / V reader is done
-    if (ld_shared_u32(sbase + L::kEpiOk) == 0u) return;
-    tc_fence_after();
-    constexpr uint32_t kOutPitch = 1024 + 16;
-    const int h = 32 * q + lane;
-    const float sc = __uint_as_float(ld_shared_u32(sbase + L::kScO + 4 * h));
-    const uint32_t lq = static_cast<uint32_t>(32 * q) << 16;
-    const bool single = p.num_splits == 1;
-    const bool f32 = !(single && !p.out_fp32);
-    const int H = p.num_heads;
-    const uint32_t stg = sbase + static_cast<uint32_t>(h) * kOutPitch;
-#pragma unroll 1
-    for (int hv = 0; hv < (f32 ? 2 : 1); ++hv) {
-#pragma unroll 1
-      for (int cc = part; cc < (f32 ? 8 : 16); cc += 3) {
-        uint32_t r[32];
-        tmem_ld32(tmem + lq + 256u * hv + 32u * cc, r);
-        tmem_ld_wait();
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]) * sc;
-        if (!f32) {
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            st_shared_v4(stg + cc * 64 + k * 16, pack_bf16x2(v[8 * k], v[8 * k + 1]),
-                         pack_bf16x2(v[8 * k + 2], v[8 * k + 3]),
-                         pack_bf16x2(v[8 * k + 4], v[8 * k + 5]),
-                         pack_bf16x2(v[8 * k + 6], v[8 * k + 7]));
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            st_shared_v4(stg + cc * 128 + k * 16, __float_as_uint(v[4 * k]),
-                         __float_as_uint(v[4 * k + 1]), __float_as_uint(v[4 * k + 2]),
-                         __float_as_uint(v[4 * k + 3]));
-        }
-      }
-      epi_sync();  // every row staged
-      // rows of 1 KB (a bf16 row or an fp32 half row)
-#pragma unroll 1
-      for (int hh = e; hh < H; hh += 12) {
-        const int64_t qhh = static_cast<int64_t>(t) * H + hh;
-        const int64_t phh = (static_cast<int64_t>(t) * p.num_splits + split) * H + hh;
-        uint8_t* dst =
-            !f32 ? reinterpret_cast<uint8_t*>(static_cast<uint16_t*>(p.out) + qhh * kLatent)
-            : single
-                ? reinterpret_cast<uint8_t*>(static_cast<float*>(p.out) + qhh * kLatent + 256 * hv)
-                : reinterpret_cast<uint8_t*>(p.ws + phh * kLatent + 256 * hv);
-        const uint32_t src = sbase + static_cast<uint32_t>(hh) * kOutPitch;
-#pragma unroll
-        for (int k = 0; k < 2; ++k)
-          *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) = ld_shared_v4(src + k * 512 + lane * 16);
-      }
-      epi_sync();  // every row written: the next half may overwrite the staging
-    }
+    epilogue_rows<L>(sbase, tmem, q, part, e, t, split, p.num_heads, p.num_splits, p.out_fp32,
+                     p.out, p.ws);
   };
-  // Score CTA: converter g (0..415) turns its share of Q (bf16, as loaded)
-  // into FP16 in place, scales folded in, heads >= H zeroed: 16-byte item i =
-  // g + 416 k is chunk i % 8 of head (i / 8) % 128 of tile i / 1024 (a quarter
-  // warp covers one 128-byte row: no bank conflicts). Then the warp signals
-  // QReady. A warp whose wait for the Q copies failed converts nothing.
   auto convert_q = [&](int g) {
-    const bool qok = warp_wait(bar(Ctl::kQFull, 0), 0, abort_addr, lim);
-    if (qok) {
-      constexpr int kItems = kQTiles * 128 * 8;
-#pragma unroll 1
-      for (int i = g; i < kItems; i += 32 * kQConverters) {
-        const int kb = i >> 10, h = (i >> 3) & 127, c = i & 7;
-        const float m = kb < 8 ? p.q_lat_mult : p.q_rope_mult;
-        const uint32_t a = sbase + L::kQ + kb * L::kQTile +
-                           sw128_off(static_cast<uint32_t>(h), static_cast<uint32_t>(c));
-        const uint4 x = h < p.num_heads ? bf16x8_to_f16x8(ld_shared_v4(a), m)
-                                        : make_uint4(0u, 0u, 0u, 0u);
-        st_shared_v4(a, x.x, x.y, x.z, x.w);
-      }
-    }
-    fence_proxy_async_cta();  // generic stores -> visible to the MMA's operand reads
-    __syncwarp();
-    if (lane == 0) mbar_arrive(bar(Ctl::kQReady, 0));
+    convert_q_share<L>(sbase, ctl, g, p.num_heads, p.q_lat_mult, p.q_rope_mult, abort_addr, lim);
   };
 
   if (gw == 0 || gw == 1) {
@@ -1118,7 +1204,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       uint32_t last_bar = 0, last_parity = 0;
       bool issued = false;
       if (rank == 0) {
-        if (wait_bar(bar(Ctl::kQReady, 0), 0, abort_addr, lim)) {
+        if (wait_bar_hot(bar(Ctl::kQReady, 0), 0, abort_addr, lim)) {
           // Operands from loop-invariant bases: the allocation of all 512
           // columns starts at TMEM address 0 (checked at set-up); a
           // descriptor's address field counts 16 bytes.
@@ -1132,13 +1218,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int i = 0; i < n_tiles && run; ++i) {
             const int s2 = i % L::kSBufs;
             const uint32_t sph = static_cast<uint32_t>(i / L::kSBufs) & 1u;
-            if (!wait_bar(bar(Ctl::kSEmpty, s2), sph ^ 1u, abort_addr, lim)) break;
+            if (!wait_bar_hot(bar(Ctl::kSEmpty, s2), sph ^ 1u, abort_addr, lim)) break;
             const uint32_t dcol = L::kSCol + 128u * s2;
             for (int kb = 0; kb < kChunksPerTile; ++kb) {
               const int q = kChunksPerTile * i + kb;
               const int cs = q % L::kKSlots;
               if (!ready &&
-                  !wait_bar(bar(Ctl::kChunkFull, cs), (q / L::kKSlots) & 1u, abort_addr, lim)) {
+                  !wait_bar_hot(bar(Ctl::kChunkFull, cs), (q / L::kKSlots) & 1u, abort_addr, lim)) {
                 run = false;
                 break;
               }
@@ -1173,14 +1259,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int vs = u % L::kVSlots;
           // P (and any rescale of O) first, then the V slot
           if (!p_ready &&
-              !wait_bar<true>(bar(Ctl::kPFull, pb), (u / kPBufs) & 1u, abort_addr, lim))
+              !wait_bar_hot<true>(bar(Ctl::kPFull, pb), (u / kPBufs) & 1u, abort_addr, lim))
             break;
           const uint4 fl = ld_shared_v4(sbase + L::kAFO + pb * kAFBytes + 512);
           if ((fl.x | fl.y | fl.z | fl.w) != 0u) {
-            if (!wait_bar(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr, lim)) break;
+            if (!wait_bar_hot(bar(Ctl::kOCorr, 0), n_corr & 1u, abort_addr, lim)) break;
             ++n_corr;
           }
-          if (!v_ready && !wait_bar(bar(Ctl::kVtFull, vs), (u / L::kVSlots) & 1u, abort_addr, lim))
+          if (!v_ready && !wait_bar_hot(bar(Ctl::kVtFull, vs), (u / L::kVSlots) & 1u, abort_addr, lim))
             break;
           tc_fence_after();
           p_ready = mbar_ready<true>(bar(Ctl::kPFull, (u + 1) % kPBufs), ((u + 1) / kPBufs) & 1u);
@@ -1219,7 +1305,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint64_t c2 = f32x2(c, c);
     const int hchunks = (p.num_heads + 31) >> 5;  // head chunks with live heads
     const uint32_t stg = sbase + L::kStg + q4 * kPiece;  // NVFP4 rows
-    const uint32_t colmax = sbase + L::kColMax + q4 * 512;
     const uint32_t peer_p = map_rank(sbase + L::kP, peer);
     const uint32_t peer_af = map_rank(sbase + L::kAFO, peer);
     const uint32_t peer_ctl = map_rank(ctl, peer);
@@ -1301,37 +1386,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (pass == 1) break;
         exceed = group_or(tmx > kTau);
         if (!exceed) break;
-        // column maxima of this warp's live rows, then per head over the four warps
-#pragma unroll 1
-        for (int hc = 0; hc < 4; ++hc) {
-          uint32_t sv[32];
-          tmem_ld32(tmem + lane_base + scol + 32u * hc, sv);
-          tmem_ld_wait();
-          float v[32];
-#pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = live ? __uint_as_float(sv[j]) : -INFINITY;
-          st_shared_u32(colmax + 4 * (32 * hc + lane), __float_as_uint(warp_colmax(v, lane)));
-        }
-        group_sync();
-        {
-          const int h = tid;
-          float mx = -INFINITY;
-#pragma unroll
-          for (int w = 0; w < 4; ++w)
-            mx = fmaxf(mx, __uint_as_float(ld_shared_u32(sbase + L::kColMax + w * 512 + 4 * h)));
-          const float mxs = mx * c;
-          const float m_old = -__uint_as_float(ld_shared_u32(sbase + L::kNegM + 4 * h));
-          float alpha = 1.f;
-          bool resc = false;
-          if (mxs > m_old + kTau) {  // also the first live score (m_old = -inf)
-            alpha = m_old == -INFINITY ? 0.f : ex2(m_old - mxs);
-            st_shared_u32(sbase + L::kNegM + 4 * h, __float_as_uint(-mxs));
-            resc = true;
-          }
-          st_shared_u32(sbase + L::kAlpha + 4 * h, __float_as_uint(alpha));
-          const bool wr = __any_sync(0xffffffffu, resc) && i > 0;
-          if (lane == 0) st_shared_u32(sbase + L::kFlags + 4 * q4, wr ? 1u : 0u);
-        }
+        // new reference maxima, their rescale factors and flags
+        softmax_new_refs<L>(sbase, tmem + lane_base + scol, live, c, i > 0);
         ok = group_and(ok);  // new references, factors and flags are visible
         if (!ok) break;
       }

@@ -42,6 +42,25 @@ def test_small_cases(num_heads, topk, seq_len, splits, padded):
     assert e < 5e-4  # fp32 output: only FP16 P rounding and fp32 accumulation remain
 
 
+# More units (query token x split) than the device holds clusters at once:
+# each cluster takes several units in turn, its barriers' phases running on
+# from one unit to the next. Every token is checked.
+@pytest.mark.parametrize("row_format", [0, 1])
+@pytest.mark.parametrize("num_heads,topk,splits,out_fp32", [
+    (64, 300, 1, False),    # 240 units of three tiles (the last one ragged), bf16 out
+    (16, 600, 2, True),     # 480 units: 240 tokens x 2 splits (the second one ragged)
+    (128, 64, 1, True),     # 240 one-tile units, full head count
+])
+def test_more_units_than_resident_clusters(row_format, num_heads, topk, splits, out_fp32):
+    wl = make_workload("tiny", num_seqs=4, seq_len=3000, num_heads=num_heads, topk=topk,
+                       q_per_seq=60)
+    case = build_case(wl, "referenced", row_format)
+    ref, ref_lse, bad = oracle_decode(case)
+    assert bad == 0
+    out, lse = gpu_decode(case, out_fp32=out_fp32, num_splits=splits)
+    assert_parity(out, lse, ref, ref_lse)
+
+
 @pytest.mark.parametrize("padded", [False, True])
 @pytest.mark.parametrize("row_format", [0, 1])
 def test_bf16_output_and_fp8_rows(row_format, padded):

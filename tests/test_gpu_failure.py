@@ -17,10 +17,15 @@ from workloads import make_workload
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("row_format,splits", [(0, 1), (0, 3), (1, 2)])
-def test_waits_that_run_out_give_nan_and_the_next_launch_is_correct(row_format, splits):
+# q_per_seq 100: 200 units, more than the device holds clusters at once, so a
+# cluster that gives up also leaves the later units it would have taken NaN
+@pytest.mark.parametrize("row_format,splits,q_per_seq", [(0, 1, 2), (0, 3, 2), (1, 2, 2),
+                                                         (0, 1, 100), (1, 1, 100)])
+def test_waits_that_run_out_give_nan_and_the_next_launch_is_correct(row_format, splits,
+                                                                     q_per_seq):
     import nvfp4_compressed_mla_gb300 as nm
-    wl = make_workload("tiny", num_seqs=2, seq_len=3000, num_heads=64, topk=900, q_per_seq=2)
+    wl = make_workload("tiny", num_seqs=2, seq_len=3000, num_heads=64, topk=900,
+                       q_per_seq=q_per_seq)
     case = build_case(wl, "referenced", row_format)
     ref, ref_lse, _ = oracle_decode(case)
     nm.nvfp4_mla_set_wait_limit(2000)
