@@ -325,29 +325,58 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride, fmt, splits,
             ws, world):
-    """Same step through the public Python API, inputs from pinned host memory each step.
+    """Same step through the C ABI with host buffers: inputs from pinned host memory each step.
 
-    Every step copies its inputs (queries, top-k, new tokens) host -> device and
-    its result (out, LSE) device -> host. The copies run on their own streams,
-    double-buffered, so step i + 1's inputs arrive and step i - 1's result
-    leaves while step i computes; events order each buffer's reuse.
+    Every step copies its inputs (queries, top-k, new tokens; packed in one
+    buffer) host -> device and its result (out and LSE; one buffer) device ->
+    host. The copies run on their own streams, double-buffered, so step i + 1's
+    inputs arrive and step i - 1's result leaves while step i computes; events
+    order each buffer's reuse. The two library calls of a step take argument
+    tuples bound once, as in the device-timed loop, so the host issues steps
+    faster than the GPU runs them (`host_ms_per_step` is the issue time).
     """
     import torch
+
+    from nvfp4_compressed_mla_gb300 import _native
+    lib = _native.load()
     layers = len(L)
     keys = ("ql", "qr", "idx", "new_lat", "new_rope")
+    offs, in_bytes = [], 0
+    for k in keys:  # 256-byte aligned slices of one buffer
+        offs.append(in_bytes)
+        t = L[0][k]
+        in_bytes += (t.numel() * t.element_size() + 255) // 256 * 256
     host = []
     for d in L:
-        host.append({k: d[k].cpu().pin_memory() for k in keys})
-    dbuf = [{k: torch.empty_like(L[0][k]) for k in keys} for _ in range(2)]
-    dout = [(torch.empty((wl.num_q, wl.num_heads, 512), dtype=torch.bfloat16, device=dev),
-             torch.empty((wl.num_q, wl.num_heads), dtype=torch.float32, device=dev))
-            for _ in range(2)]
-    hout = [(torch.empty((wl.num_q, wl.num_heads, 512), dtype=torch.bfloat16).pin_memory(),
-             torch.empty((wl.num_q, wl.num_heads), dtype=torch.float32).pin_memory())
-            for _ in range(2)]
-    h2d = sum(v.numel() * v.element_size() for v in host[0].values())
-    d2h = hout[0][0].numel() * 2 + hout[0][1].numel() * 4
+        hb = torch.zeros(in_bytes, dtype=torch.uint8).pin_memory()
+        for k, o in zip(keys, offs):
+            src = d[k].contiguous().view(torch.uint8).reshape(-1).cpu()
+            hb[o:o + src.numel()].copy_(src)
+        host.append(hb)
+    dbuf = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    out_bytes = wl.num_q * wl.num_heads * 512 * 2
+    lse_off = (out_bytes + 255) // 256 * 256
+    res_bytes = lse_off + wl.num_q * wl.num_heads * 4
+    dres = [torch.empty(res_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    hres = [torch.empty(res_bytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
     comp = torch.cuda.current_stream(dev)
+    sh = comp.cuda_stream
+    n_app = int(app_seq.numel())
+    app, dec = {}, {}
+    for li in range(layers):
+        for b in range(2):
+            ptr = {k: dbuf[b].data_ptr() + o for k, o in zip(keys, offs)}
+            pool = L[li]["pool"].data_ptr()
+            app[li, b] = (ptr["new_lat"], ptr["new_rope"], app_seq.data_ptr(), app_pos.data_ptr(),
+                          n_app, bt.data_ptr(), wl.num_seqs, wl.max_blocks_per_seq, 64, pool,
+                          wl.num_blocks, stride, fmt, 1.0, 1.0, None, sh)
+            dec[li, b] = (ptr["ql"], ptr["qr"], q_seq.data_ptr(), ptr["idx"], wl.num_q,
+                          wl.num_heads, wl.topk, bt.data_ptr(), wl.num_seqs,
+                          wl.max_blocks_per_seq, seq_lens.data_ptr(), 64, pool, wl.num_blocks,
+                          stride, fmt, wl.sm_scale, 1.0, 1.0, dres[b].data_ptr(), 0,
+                          dres[b].data_ptr() + lse_off, ws.data_ptr(), ws.numel(), splits, None,
+                          sh)
+    append_fn, decode_fn = lib.nvfp4_mla_append, lib.sparse_mla_decode
     cin, cout = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev = lambda: torch.cuda.Event()  # noqa: E731
     in_ready = [ev(), ev()]
@@ -359,27 +388,21 @@ def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride,
 
     def step(i):
         b = i & 1
-        h = host[i % layers]
-        with torch.cuda.stream(cin):           # inputs of step i into buffer b
-            cin.wait_event(used[b])
-            for k in keys:
-                dbuf[b][k].copy_(h[k], non_blocking=True)
-            in_ready[b].record(cin)
+        li = i % layers
+        cin.wait_event(used[b])               # inputs of step i into buffer b
+        with torch.cuda.stream(cin):
+            dbuf[b].copy_(host[li], non_blocking=True)
+        in_ready[b].record(cin)
         comp.wait_event(in_ready[b])
-        comp.wait_event(out_read[b])           # buffer b's previous result has been read
-        d = dbuf[b]
-        nm.nvfp4_mla_append(d["new_lat"], d["new_rope"], app_seq, app_pos, bt, 64,
-                            L[i % layers]["pool"], wl.num_blocks, stride, fmt, stream=comp)
-        nm.sparse_mla_decode(d["ql"], d["qr"], q_seq, d["idx"], bt, seq_lens, 64,
-                             L[i % layers]["pool"], wl.num_blocks, stride, fmt, wl.sm_scale,
-                             out=dout[b][0], lse=dout[b][1], workspace=ws, num_splits=splits,
-                             stream=comp)
+        comp.wait_event(out_read[b])          # buffer b's previous result has been read
+        a, c = append_fn(*app[li, b]), decode_fn(*dec[li, b])
+        if a or c:
+            raise RuntimeError(f"status append={a} decode={c}")
         used[b].record(comp)
-        with torch.cuda.stream(cout):          # result of step i to the host
-            cout.wait_event(used[b])
-            hout[b][0].copy_(dout[b][0], non_blocking=True)
-            hout[b][1].copy_(dout[b][1], non_blocking=True)
-            out_read[b].record(cout)
+        cout.wait_event(used[b])              # result of step i to the host
+        with torch.cuda.stream(cout):
+            hres[b].copy_(dres[b], non_blocking=True)
+        out_read[b].record(cout)
 
     for i in range(5):
         step(i)
@@ -390,8 +413,10 @@ def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride,
         torch.distributed.barrier()
     torch.cuda.synchronize()
     s.record(comp)
+    t0 = time.perf_counter()
     for i in range(K):
         step(i)
+    host_ms = (time.perf_counter() - t0) * 1e3
     comp.wait_event(out_read[0])
     comp.wait_event(out_read[1])
     e.record(comp)
@@ -399,9 +424,10 @@ def run_e2e(args, wl, L, nm, dev, bt, seq_lens, q_seq, app_seq, app_pos, stride,
     ms = max_over_ranks(s.elapsed_time(e), world, dev)
     kv = wl.valid_slots() * ROW_BYTES[fmt]
     return {"value": round(whole_job_gbs(kv, K, world, ms), 3), "unit": "GB/s",
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
-            "ms_per_step": round(ms / K, 5),
-            "copies": "host->device and device->host on their own streams, double-buffered"}
+            "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": res_bytes, "steps": K,
+            "ms_per_step": round(ms / K, 5), "host_ms_per_step": round(host_ms / K, 5),
+            "copies": "one host->device and one device->host copy per step on their own "
+                      "streams, double-buffered"}
 
 
 # ------------------------------------------------------------ CPU oracle
