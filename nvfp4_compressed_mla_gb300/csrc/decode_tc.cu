@@ -128,11 +128,13 @@ struct TcLayout {
   static constexpr int kStageO = (kSub / 4) * kGroupO;
   // P^T pieces reach the output CTA either through a local staging slot and
   // one bulk copy per piece (NVFP4 rows), or as the softmax warps' own stores
-  // into the peer (FP8 rows: the staging's 32 KB buy the score CTA's ring a
-  // third stage of the wider rows instead; the stores are slower, the deeper
-  // gather prefetch wins for those rows).
+  // into the peer (FP8 rows: the staging's 32 KB buy the score CTA's ring
+  // stages of the wider rows instead; the stores are slower, the deeper
+  // gather prefetch wins for those rows). The score CTA's ring holds four
+  // stages (one tile) in both formats; the output CTA's three FP8 stages
+  // measure as fast as four.
   static constexpr bool kDirectP = !kNv;
-  static constexpr int kStagesS = kNv ? 4 : 3;
+  static constexpr int kStagesS = 4;
   static constexpr int kStagesO = kNv ? 4 : 3;
   // score CTA
   static constexpr int kQTile = 16384;                      // 128 heads x 64 dims (SW128)
