@@ -1296,7 +1296,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ score CTA: Q set-up, then softmax
     const int q4 = warp;  // quadrant: rows 32 q4 .. + 31 of each tile
     const uint32_t lane_base = static_cast<uint32_t>(32 * q4) << 16;
-    bool ok;
+    // `ok` is the same in the four warps (it changes only at their group
+    // barriers, so they all pass the same barriers in the same order); `sent`
+    // is this warp's own: whether its waits for the peer's P buffers held. A
+    // warp whose wait ran out stores nothing more into the peer and follows
+    // the others to the next group barrier, where they all stop.
+    bool ok, sent = true;
     {
       // this warp's share of Q, then the initial reference maxima
       st_shared_u32(sbase + L::kNegM + 4 * tid, __float_as_uint(INFINITY));  // m_ref = -inf
@@ -1342,9 +1347,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int cc = 0; cc < 4; ++cc) {
         const uint32_t a = blk + sw128_off(static_cast<uint32_t>(lane), 4 * (hc & 1) + cc);
-        if constexpr (L::kDirectP)
-          st_cluster_v4(a, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
-        else
+        if constexpr (L::kDirectP) {
+          if (sent) st_cluster_v4(a, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
+        } else
           st_shared_v4(a, pk[4 * cc], pk[4 * cc + 1], pk[4 * cc + 2], pk[4 * cc + 3]);
       }
       return live ? tmx : -INFINITY;
@@ -1352,7 +1357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     for (int i = 0; i < n_tiles && ok; ++i) {
       const int s2 = i % L::kSBufs;
       const uint32_t scol = L::kSCol + 128u * s2;
-      ok = group_and(wait_bar(bar(Ctl::kSFull, s2), (i / L::kSBufs) & 1u, abort_addr, lim));
+      ok = group_and(sent && wait_bar(bar(Ctl::kSFull, s2), (i / L::kSBufs) & 1u, abort_addr, lim));
       if (!ok) break;
       tc_fence_after();
       const int u = kPiecesPerTile * i + q4;
@@ -1366,8 +1371,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0)
           free_ok = wait_bar<true>(bar(Ctl::kPEmpty, pb), ((u / kPBufs) & 1u) ^ 1u, abort_addr, lim)
                         ? 1u : 0u;
-        ok = __shfl_sync(0xffffffffu, free_ok, 0) != 0u;
-        if (!ok) break;
+        sent = __shfl_sync(0xffffffffu, free_ok, 0) != 0u;
         dst = peer_p + static_cast<uint32_t>(pb) * kPiece;
       } else {
         // this warp's staging slot: its copy of the previous tile has read it
@@ -1399,6 +1403,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(Ctl::kSEmpty, s2));
       if constexpr (L::kDirectP) {
+        if (!sent) continue;
         // factors (tile's first piece) or zero flags straight into the peer's
         // factor block; every lane releases its stores and arrives
         const uint32_t af = peer_af + static_cast<uint32_t>(pb) * kAFBytes;
@@ -1453,10 +1458,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           st_shared_u32(ctl + Ctl::kSentCnt + 4 * pb, static_cast<uint32_t>(u / kPBufs + 1));
         }
       }
-      ok = __shfl_sync(0xffffffffu, sent_ok, 0) != 0u;
+      sent = __shfl_sync(0xffffffffu, sent_ok, 0) != 0u;
     }
     if (lane == 0) bulk_wait_read<0>();  // every copy has read this warp's slot
-    ok = group_and(ok);
+    ok = group_and(ok && sent);
     // the peer learns how many pieces went into each P buffer (it drains them
     // on abort), then the final reference maximum of head h = tid
     if (tid == 0 && !L::kDirectP) {
