@@ -16,7 +16,7 @@
 //   rank 0, "score" CTA: S^T = K Q^T per 128-row tile (M = 128 rows,
 //     N = the heads rounded up to 32, K = 576). The dequant warps expand the gathered rows
 //     (thread = row) straight into tensor memory, where they are the MMA's A
-//     operand: a ring of 64-dimension chunks, so the FP16 K tile never
+//     operand: a ring of 128-dimension chunks, so the FP16 K tile never
 //     touches shared memory. Q (FP16, all 576 dimensions of the 128 heads)
 //     stays resident in shared memory as the B operand; it arrives by nine
 //     2-D tensor copies and is converted in place. Four softmax warps
@@ -33,8 +33,8 @@
 //
 // Both CTAs gather their own copy of the rows: two gather warps take
 // alternate 32-slot stages, resolve the stage's top-k slots through the block
-// table (-1 and unresolvable slots issue no load; the index and block-table
-// loads run two of the warp's stages ahead), publish the stage's live-row
+// table (-1 and unresolvable slots issue no load; the index loads run four
+// of the warp's stages ahead, the block-table loads two), publish the stage's live-row
 // mask and copy the live rows with tile::gather4 tensor copies (four rows per
 // copy; one bulk copy per row when the page stride is not a whole number of
 // rows). Every wait is bounded; a
